@@ -229,6 +229,26 @@ def attention(q: np.ndarray, k: np.ndarray, v: np.ndarray, n_heads: int,
     return out.reshape(n, n_heads * d)
 
 
+def attention_rows(q_rows: np.ndarray, k: np.ndarray, v: np.ndarray, n_heads: int,
+                   n_kv_heads: int) -> np.ndarray:
+    """The same attention for a subset of query rows of one sequence:
+    q_rows [R, n_heads, d] attend to all keys k, v [S, n_kv_heads, d].  Each
+    output row depends only on its own query, so this equals the matching
+    rows of attention() (pinned by a test).  Returns [R, n_heads * d]."""
+    r, _, d = q_rows.shape
+    group = n_heads // n_kv_heads
+    scale = F32(1.0 / math.sqrt(d))
+    out = np.empty((r, n_heads, d), dtype=F32)
+    for h in range(n_heads):
+        g = h // group
+        sc = np.matmul(q_rows[:, h, :], k[:, g, :].T).astype(F32) * scale
+        sc = sc - sc.max(axis=1, keepdims=True)
+        p = np.exp(sc).astype(F32)
+        p = p / p.sum(axis=1, keepdims=True, dtype=F32)
+        out[:, h, :] = np.matmul(p, v[:, g, :])
+    return out.reshape(r, n_heads * d)
+
+
 # --------------------------------------------------------------------------
 # One block
 # --------------------------------------------------------------------------
@@ -287,6 +307,32 @@ def block_forward(cfg: BlockConfig, w: dict, x: np.ndarray,
     h = silu(gu[:, :f]) * gu[:, f:]
     x = gated_residual(x, gate2, linear(h.astype(F32), w["w_down"]))
     return x
+
+
+def block_forward_rows(cfg: BlockConfig, w: dict, x: np.ndarray, mod: Optional[np.ndarray],
+                       angles: np.ndarray, rows: np.ndarray) -> np.ndarray:
+    """block_forward restricted to some output rows of a single sequence:
+    keys and values come from every row, everything after attention is
+    per-row.  Same steps and order as block_forward; returns [len(rows), H]
+    (pinned against block_forward by a test)."""
+    x = x.astype(F32, copy=False)
+    if cfg.adaln:
+        shift1, scale1, gate1, shift2, scale2, gate2 = (mod[i] for i in range(6))
+        a = modulate(layer_norm(x, cfg.ln_eps), shift1, scale1)
+    else:
+        gate1 = gate2 = None
+        a = layer_norm(x, cfg.ln_eps) * w["ln1_g"] + w["ln1_b"]
+    q, k, v = qkv_heads(cfg, a, w, angles)
+    o = attention_rows(q[rows], k, v, cfg.n_heads, cfg.n_kv_heads)
+    xr = gated_residual(x[rows], gate1, linear(o, w["w_o"]))
+    if cfg.adaln:
+        a2 = modulate(layer_norm(xr, cfg.ln_eps), shift2, scale2)
+    else:
+        a2 = layer_norm(xr, cfg.ln_eps) * w["ln2_g"] + w["ln2_b"]
+    gu = linear(a2, w["w_gu"])
+    f = cfg.ffn
+    h = silu(gu[:, :f]) * gu[:, f:]
+    return gated_residual(xr, gate2, linear(h.astype(F32), w["w_down"]))
 
 
 # --------------------------------------------------------------------------

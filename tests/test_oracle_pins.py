@@ -429,3 +429,22 @@ def test_block_attention_branch_closed_form():
     branch = (mod[0].astype(np.float64) @ wv.T.astype(np.float64)) @ w["w_o"].T.astype(np.float64)
     expect = x + mod[2] * branch[None, :]
     np.testing.assert_allclose(O.block_forward(cfg, w, x, mod, ang), expect, rtol=1e-5, atol=1e-5)
+
+
+def test_attention_rows_matches_attention():
+    q, k, v = rnd(9, 4, 8), rnd(9, 2, 8), rnd(9, 2, 8)
+    rows = np.array([0, 4, 8, 3])
+    np.testing.assert_allclose(O.attention_rows(q[rows], k, v, 4, 2), O.attention(q, k, v, 4, 2)[rows],
+                               rtol=1e-6, atol=1e-7)
+
+
+@pytest.mark.parametrize("adaln", [True, False])
+def test_block_forward_rows_matches_block_forward(adaln):
+    cfg = tiny_cfg(adaln=adaln, qk_norm=adaln)
+    w = tiny_weights(cfg)
+    x, mod, pos = tiny_inputs()
+    ang = O.rope_angles_3d(pos, AXES, 256.0)
+    rows = np.array([1, 14, 0, 7])
+    full = O.block_forward(cfg, w, x, mod if adaln else None, ang)
+    np.testing.assert_allclose(O.block_forward_rows(cfg, w, x, mod if adaln else None, ang, rows),
+                               full[rows], rtol=1e-5, atol=1e-5)
