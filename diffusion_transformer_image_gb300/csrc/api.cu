@@ -1,0 +1,589 @@
+// The C ABI of libdit.so: argument checks, workspace layout and the order in
+// which the kernels of one block and one denoise step are enqueued.
+#include <math.h>
+#include <string.h>
+
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "internal.h"
+
+namespace dit {
+
+// The device error word that every bounded in-kernel wait reports to.
+__device__ int g_dit_error_word;
+
+namespace {
+
+constexpr int MAX_DEVICES = 64;
+DeviceState g_states[MAX_DEVICES];
+bool g_ready[MAX_DEVICES];
+std::mutex g_mu;
+thread_local int64_t t_launches = 0;
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+size_t align256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
+
+dit_status cuda_status(cudaError_t e) { return e == cudaSuccess ? DIT_OK : DIT_ECUDA; }
+
+}  // namespace
+
+const DeviceState* device_state() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= MAX_DEVICES) return nullptr;
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (!g_ready[dev]) {
+    DeviceState s{};
+    if (cudaDeviceGetAttribute(&s.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return nullptr;
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_dit_error_word) != cudaSuccess) return nullptr;
+    s.err = static_cast<int*>(p);
+    s.timeout_ns = 2000000000ull;
+    if (g_encode == nullptr) {
+      void* fn = nullptr;
+      cudaDriverEntryPointQueryResult q;
+      if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                           cudaEnableDefault, &q) != cudaSuccess ||
+          q != cudaDriverEntryPointSuccess || fn == nullptr)
+        return nullptr;
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+    g_states[dev] = s;
+    g_ready[dev] = true;
+  }
+  return &g_states[dev];
+}
+
+void count_launch(int n) { t_launches += n; }
+
+bool make_tmap_bf16(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
+                    const uint64_t* strides_bytes, const uint32_t* box) {
+  if (g_encode == nullptr || !aligned16(base)) return false;
+  cuuint64_t gd[5];
+  cuuint64_t gs[4];
+  cuuint32_t bx[5];
+  cuuint32_t es[5];
+  for (int i = 0; i < rank; ++i) {
+    gd[i] = dims[i];
+    bx[i] = box[i];
+    es[i] = 1;
+    if (i + 1 < rank) {
+      if (strides_bytes[i] % 16 != 0) return false;
+      gs[i] = strides_bytes[i];
+    }
+  }
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank,
+                        const_cast<void*>(base), gd, gs, bx, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+namespace {
+
+// ------------------------------------------------------------ validation
+dit_status check_block_config(const dit_block_config* c) {
+  if (!c) return DIT_EINVAL;
+  if (c->hidden <= 0 || c->n_heads <= 0 || c->n_kv_heads <= 0 || c->ffn <= 0) return DIT_EINVAL;
+  if (c->head_dim != 64 && c->head_dim != 128) return DIT_EUNSUPPORTED;
+  if (c->hidden % 64 != 0 || c->hidden > 8192) return DIT_EUNSUPPORTED;
+  if (c->n_heads % c->n_kv_heads != 0) return DIT_EUNSUPPORTED;
+  if (c->ffn % 128 != 0) return DIT_EUNSUPPORTED;
+  if (c->rope_layout != 0 && c->rope_layout != 1) return DIT_EINVAL;
+  if (!(c->ln_eps >= 0.0f)) return DIT_EINVAL;
+  return DIT_OK;
+}
+
+struct BlockWs {
+  __nv_bfloat16 *a, *qk, *vt, *o, *h;
+  size_t bytes;
+};
+
+BlockWs block_ws_layout(const dit_block_config* c, int n_tokens, int n_seqs, void* base) {
+  const size_t N = (size_t)n_tokens;
+  const size_t s_len = N / (size_t)n_seqs;
+  const size_t s_pad = (s_len + 7) & ~static_cast<size_t>(7);
+  const size_t hd = (size_t)c->head_dim;
+  size_t off = 0;
+  BlockWs w{};
+  auto take = [&](size_t bytes) {
+    uint8_t* p = base ? static_cast<uint8_t*>(base) + off : nullptr;
+    off += align256(bytes);
+    return reinterpret_cast<__nv_bfloat16*>(p);
+  };
+  w.a = take(N * c->hidden * 2);
+  w.qk = take(N * (size_t)(c->n_heads + c->n_kv_heads) * hd * 2);
+  w.vt = take((size_t)n_seqs * c->n_kv_heads * hd * s_pad * 2);
+  w.o = take(N * (size_t)c->n_heads * hd * 2);
+  w.h = take(N * (size_t)c->ffn * 2);
+  w.bytes = off;
+  return w;
+}
+
+dit_status run_qkv(const dit_block_config* c, const dit_block_weights* w, const void* a,
+                   int n_tokens, int n_seqs, const float* rc, const float* rs,
+                   __nv_bfloat16* qk, __nv_bfloat16* vt, cudaStream_t st) {
+  const int hd = c->head_dim;
+  GemmParams p{};
+  p.M = n_tokens;
+  p.N = (c->n_heads + 2 * c->n_kv_heads) * hd;
+  p.K = c->hidden;
+  p.qkv.qk = qk;
+  p.qkv.ldqk = (c->n_heads + c->n_kv_heads) * hd;
+  p.qkv.vt = vt;
+  p.qkv.s_len = n_tokens / n_seqs;
+  p.qkv.s_pad = (p.qkv.s_len + 7) & ~7;
+  p.qkv.nh = c->n_heads;
+  p.qkv.nkv = c->n_kv_heads;
+  if (c->qk_norm) {
+    p.qkv.qg = w->q_g;
+    p.qkv.qb = w->q_b;
+    p.qkv.kg = w->k_g;
+    p.qkv.kb = w->k_b;
+  }
+  p.qkv.rcos = rc;
+  p.qkv.rsin = rs;
+  p.qkv.rope_half = c->rope_layout;
+  p.qkv.eps = c->ln_eps;
+  return cuda_status(launch_gemm(EPI_QKV, hd, a, c->hidden, w->w_qkv, c->hidden, p, st));
+}
+
+dit_status block_forward_impl(const dit_block_config* c, const dit_block_weights* w, float* x,
+                              int n_tokens, int n_seqs, const float* mod, const float* rc,
+                              const float* rs, const BlockWs& ws, cudaStream_t st) {
+  const int H = c->hidden, hd = c->head_dim, F = c->ffn;
+  const bool ada = c->adaln != 0;
+  cudaError_t e;
+  // a = LN(x) (1 + scale1) + shift1   |   LN(x) g1 + b1
+  e = launch_ln_modulate(ada ? 0 : 1, x, H, n_tokens, H, ada ? mod : w->ln1_g,
+                         ada ? mod + H : w->ln1_b, c->ln_eps, ws.a, H, st);
+  if (e != cudaSuccess) return DIT_ECUDA;
+  dit_status s = run_qkv(c, w, ws.a, n_tokens, n_seqs, rc, rs, ws.qk, ws.vt, st);
+  if (s != DIT_OK) return s;
+  e = launch_attention(hd, ws.qk, ws.vt, n_tokens, n_seqs, c->n_heads, c->n_kv_heads, ws.o, st);
+  if (e != cudaSuccess) return DIT_ECUDA;
+  {  // x += gate1 (o Wo^T)
+    GemmParams p{};
+    p.M = n_tokens;
+    p.N = H;
+    p.K = c->n_heads * hd;
+    p.out = x;
+    p.ldo = H;
+    p.vec = ada ? mod + 2 * H : nullptr;
+    e = launch_gemm(EPI_RESIDUAL, 0, ws.o, p.K, w->w_o, p.K, p, st);
+    if (e != cudaSuccess) return DIT_ECUDA;
+  }
+  e = launch_ln_modulate(ada ? 0 : 1, x, H, n_tokens, H, ada ? mod + 3 * H : w->ln2_g,
+                         ada ? mod + 4 * H : w->ln2_b, c->ln_eps, ws.a, H, st);
+  if (e != cudaSuccess) return DIT_ECUDA;
+  {  // h = SiLU(a Wg^T) (a Wu^T)
+    GemmParams p{};
+    p.M = n_tokens;
+    p.N = F;
+    p.K = H;
+    p.out = ws.h;
+    p.ldo = F;
+    e = launch_gemm(EPI_SWIGLU, 0, ws.a, H, w->w_gu, H, p, st);
+    if (e != cudaSuccess) return DIT_ECUDA;
+  }
+  {  // x += gate2 (h Wd^T)
+    GemmParams p{};
+    p.M = n_tokens;
+    p.N = H;
+    p.K = F;
+    p.out = x;
+    p.ldo = H;
+    p.vec = ada ? mod + 5 * H : nullptr;
+    e = launch_gemm(EPI_RESIDUAL, 0, ws.h, F, w->w_down, F, p, st);
+    if (e != cudaSuccess) return DIT_ECUDA;
+  }
+  return DIT_OK;
+}
+
+dit_status check_block_weights(const dit_block_config* c, const dit_block_weights* w) {
+  if (!w || !w->w_qkv || !w->w_o || !w->w_gu || !w->w_down) return DIT_EINVAL;
+  if (!aligned16(w->w_qkv) || !aligned16(w->w_o) || !aligned16(w->w_gu) || !aligned16(w->w_down))
+    return DIT_EINVAL;
+  if (c->qk_norm && (!w->q_g || !w->q_b || !w->k_g || !w->k_b)) return DIT_EINVAL;
+  if (!c->adaln) {
+    if (!w->ln1_g || !w->ln1_b || !w->ln2_g || !w->ln2_b) return DIT_EINVAL;
+    if (!aligned16(w->ln1_g) || !aligned16(w->ln1_b) || !aligned16(w->ln2_g) ||
+        !aligned16(w->ln2_b))
+      return DIT_EINVAL;
+  }
+  return DIT_OK;
+}
+
+struct StepWs {
+  float *x, *rcos, *rsin, *cond, *mod, *fin, *v;
+  __nv_bfloat16* lat;
+  void* block;
+  size_t block_bytes;
+  size_t bytes;
+};
+
+StepWs step_ws_layout(const dit_model_config* m, int grid_h, int grid_w, int n_txt, void* base) {
+  const dit_block_config* c = &m->block;
+  const size_t n_img = (size_t)grid_h * grid_w;
+  const size_t N = n_img + (size_t)n_txt;
+  const size_t H = (size_t)c->hidden;
+  const size_t C = (size_t)m->latent_channels;
+  size_t off = 0;
+  StepWs w{};
+  auto take = [&](size_t bytes) {
+    uint8_t* p = base ? static_cast<uint8_t*>(base) + off : nullptr;
+    off += align256(bytes);
+    return p;
+  };
+  w.x = reinterpret_cast<float*>(take(N * H * 4));
+  w.rcos = reinterpret_cast<float*>(take(N * (size_t)(c->head_dim / 2) * 4));
+  w.rsin = reinterpret_cast<float*>(take(N * (size_t)(c->head_dim / 2) * 4));
+  w.cond = reinterpret_cast<float*>(take(((size_t)m->t_dim + 2 * H) * 4));
+  w.mod = reinterpret_cast<float*>(take(6 * H * 4));
+  w.fin = reinterpret_cast<float*>(take(2 * H * 4));
+  w.v = reinterpret_cast<float*>(take(n_img * C * 4));
+  w.lat = reinterpret_cast<__nv_bfloat16*>(take(n_img * C * 2));
+  BlockWs b = block_ws_layout(c, (int)N, 1, nullptr);
+  w.block = take(b.bytes);
+  w.block_bytes = b.bytes;
+  w.bytes = off;
+  return w;
+}
+
+dit_status check_model(const dit_model_config* m) {
+  if (!m) return DIT_EINVAL;
+  dit_status s = check_block_config(&m->block);
+  if (s != DIT_OK) return s;
+  if (!m->block.adaln) return DIT_EUNSUPPORTED;
+  if (m->n_layers < 0 || m->latent_channels <= 0 || m->t_dim <= 0 || m->t_dim % 8 != 0)
+    return DIT_EINVAL;
+  if (m->latent_channels % 8 != 0) return DIT_EUNSUPPORTED;
+  const int half = m->block.head_dim / 2;
+  if (m->rope_axes[0] % 2 || m->rope_axes[1] % 2 || m->rope_axes[2] % 2 ||
+      (m->rope_axes[0] + m->rope_axes[1] + m->rope_axes[2]) / 2 != half)
+    return DIT_EINVAL;
+  return DIT_OK;
+}
+
+dit_status conditioning_impl(const dit_model_config* m, const dit_model_weights* w, float sigma,
+                             float* mod, float* fin, float* scratch, cudaStream_t st) {
+  const int H = m->block.hidden;
+  float* e = scratch;
+  float* h1 = scratch + m->t_dim;
+  float* temb = h1 + H;
+  const float T = m->t_scale * sigma;
+  cudaError_t r;
+  if ((r = launch_sinusoid(T, m->t_dim, e, st)) != cudaSuccess) return DIT_ECUDA;
+  if ((r = launch_gemv(static_cast<const __nv_bfloat16*>(w->t_w1), e, w->t_b1, h1, H, m->t_dim, 0,
+                       st)) != cudaSuccess)
+    return DIT_ECUDA;
+  if ((r = launch_gemv(static_cast<const __nv_bfloat16*>(w->t_w2), h1, w->t_b2, temb, H, H, 1,
+                       st)) != cudaSuccess)
+    return DIT_ECUDA;
+  if ((r = launch_gemv(static_cast<const __nv_bfloat16*>(w->mod_w), temb, w->mod_b, mod, 6 * H, H,
+                       1, st)) != cudaSuccess)
+    return DIT_ECUDA;
+  if ((r = launch_gemv(static_cast<const __nv_bfloat16*>(w->fin_w), temb, w->fin_b, fin, 2 * H, H,
+                       1, st)) != cudaSuccess)
+    return DIT_ECUDA;
+  return DIT_OK;
+}
+
+dit_status check_model_weights(const dit_model_config* m, const dit_model_weights* w) {
+  if (!w || !w->patch_w || !w->t_w1 || !w->t_w2 || !w->mod_w || !w->fin_w || !w->out_w)
+    return DIT_EINVAL;
+  if (!aligned16(w->patch_w) || !aligned16(w->out_w) || !aligned16(w->t_w1) ||
+      !aligned16(w->t_w2) || !aligned16(w->mod_w) || !aligned16(w->fin_w))
+    return DIT_EINVAL;
+  if (m->n_layers > 0 && !w->layers) return DIT_EINVAL;
+  for (int l = 0; l < m->n_layers; ++l) {
+    dit_status s = check_block_weights(&m->block, &w->layers[l]);
+    if (s != DIT_OK) return s;
+  }
+  return DIT_OK;
+}
+
+}  // namespace
+}  // namespace dit
+
+using namespace dit;
+
+extern "C" {
+
+size_t dit_block_workspace_bytes(const dit_block_config* cfg, int32_t n_tokens, int32_t n_seqs) {
+  if (check_block_config(cfg) != DIT_OK || n_tokens <= 0 || n_seqs <= 0 || n_tokens % n_seqs)
+    return 0;
+  return block_ws_layout(cfg, n_tokens, n_seqs, nullptr).bytes;
+}
+
+dit_status dit_block_forward(const dit_block_config* cfg, const dit_block_weights* w, float* x,
+                             int32_t n_tokens, int32_t n_seqs, const float* mod,
+                             const float* rope_cos, const float* rope_sin, void* workspace,
+                             size_t ws_bytes, void* stream) {
+  dit_status s = check_block_config(cfg);
+  if (s != DIT_OK) return s;
+  if ((s = check_block_weights(cfg, w)) != DIT_OK) return s;
+  if (!x || n_tokens <= 0 || n_seqs <= 0 || n_tokens % n_seqs) return DIT_EINVAL;
+  if (!aligned16(x) || !rope_cos || !rope_sin || !aligned16(rope_cos) || !aligned16(rope_sin))
+    return DIT_EINVAL;
+  if (cfg->adaln && (!mod || !aligned16(mod))) return DIT_EINVAL;
+  if (!workspace || !aligned16(workspace)) return DIT_EINVAL;
+  BlockWs ws = block_ws_layout(cfg, n_tokens, n_seqs, workspace);
+  if (ws_bytes < ws.bytes) return DIT_EWORKSPACE;
+  if (!device_state()) return DIT_ECUDA;
+  return block_forward_impl(cfg, w, x, n_tokens, n_seqs, mod, rope_cos, rope_sin, ws,
+                            static_cast<cudaStream_t>(stream));
+}
+
+size_t dit_denoise_workspace_bytes(const dit_model_config* cfg, int32_t grid_h, int32_t grid_w,
+                                   int32_t n_txt) {
+  if (check_model(cfg) != DIT_OK || grid_h <= 0 || grid_w <= 0 || n_txt < 0) return 0;
+  return step_ws_layout(cfg, grid_h, grid_w, n_txt, nullptr).bytes;
+}
+
+dit_status dit_denoise_step(const dit_model_config* cfg, const dit_model_weights* w,
+                            float* latent, const void* text, int32_t grid_h, int32_t grid_w,
+                            int32_t n_txt, float sigma, float sigma_next, float* velocity_out,
+                            void* workspace, size_t ws_bytes, void* stream) {
+  dit_status s = check_model(cfg);
+  if (s != DIT_OK) return s;
+  if ((s = check_model_weights(cfg, w)) != DIT_OK) return s;
+  if (!latent || !aligned16(latent) || grid_h <= 0 || grid_w <= 0 || n_txt < 0) return DIT_EINVAL;
+  if (n_txt > 0 && (!text || !aligned16(text))) return DIT_EINVAL;
+  if (velocity_out && !aligned16(velocity_out)) return DIT_EINVAL;
+  if (!workspace || !aligned16(workspace)) return DIT_EINVAL;
+  StepWs ws = step_ws_layout(cfg, grid_h, grid_w, n_txt, workspace);
+  if (ws_bytes < ws.bytes) return DIT_EWORKSPACE;
+  if (!device_state()) return DIT_ECUDA;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const dit_block_config* c = &cfg->block;
+  const int H = c->hidden, C = cfg->latent_channels;
+  const int n_img = grid_h * grid_w;
+  const int N = n_img + n_txt;
+
+  if ((s = conditioning_impl(cfg, w, sigma, ws.mod, ws.fin, ws.cond, st)) != DIT_OK) return s;
+  // x[0:n_img] = latent Wp^T + bp  (latent rounded to bf16 for the tensor core)
+  if (launch_f32_to_bf16(latent, ws.lat, (long long)n_img * C, st) != cudaSuccess) return DIT_ECUDA;
+  {
+    GemmParams p{};
+    p.M = n_img;
+    p.N = H;
+    p.K = C;
+    p.out = ws.x;
+    p.ldo = H;
+    p.vec = w->patch_b;
+    if (launch_gemm(EPI_F32_BIAS, 0, ws.lat, C, w->patch_w, C, p, st) != cudaSuccess)
+      return DIT_ECUDA;
+  }
+  // x[n_img:] = text
+  if (n_txt > 0 &&
+      launch_bf16_to_f32(static_cast<const __nv_bfloat16*>(text), ws.x + (size_t)n_img * H,
+                         (long long)n_txt * H, st) != cudaSuccess)
+    return DIT_ECUDA;
+  if (launch_rope_grid(grid_h, grid_w, n_txt, nullptr, 0, cfg->rope_axes, cfg->rope_theta,
+                       c->head_dim / 2, ws.rcos, ws.rsin, st) != cudaSuccess)
+    return DIT_ECUDA;
+  BlockWs bws = block_ws_layout(c, N, 1, ws.block);
+  for (int l = 0; l < cfg->n_layers; ++l) {
+    s = block_forward_impl(c, &w->layers[l], ws.x, N, 1, ws.mod, ws.rcos, ws.rsin, bws, st);
+    if (s != DIT_OK) return s;
+  }
+  // v = (LN(x_img) (1 + scale_f) + shift_f) Wout^T + bout; fin = [scale, shift]
+  if (launch_ln_modulate(0, ws.x, H, n_img, H, ws.fin + H, ws.fin, c->ln_eps, bws.a, H, st) !=
+      cudaSuccess)
+    return DIT_ECUDA;
+  float* v = velocity_out ? velocity_out : ws.v;
+  {
+    GemmParams p{};
+    p.M = n_img;
+    p.N = C;
+    p.K = H;
+    p.out = v;
+    p.ldo = C;
+    p.vec = w->out_b;
+    if (launch_gemm(EPI_F32_BIAS, 0, bws.a, H, w->out_w, H, p, st) != cudaSuccess)
+      return DIT_ECUDA;
+  }
+  const float dt = sigma_next - sigma;
+  return cuda_status(launch_euler(latent, v, (long long)n_img * C, dt, st));
+}
+
+dit_status flowmatch_euler_step(float* x, const float* v, int64_t n, float sigma,
+                                float sigma_next, void* stream) {
+  if (n < 0 || (n > 0 && (!x || !v || !aligned16(x) || !aligned16(v)))) return DIT_EINVAL;
+  if (!device_state()) return DIT_ECUDA;
+  return cuda_status(launch_euler(x, v, n, sigma_next - sigma, static_cast<cudaStream_t>(stream)));
+}
+
+dit_status flowmatch_sigmas(int32_t n_steps, float shift, float* out_host) {
+  if (n_steps <= 0 || !out_host || !(shift > 0.0f)) return DIT_EINVAL;
+  for (int i = 0; i <= n_steps; ++i) {
+    const double s = 1.0 - (double)i / (double)n_steps;
+    out_host[i] = (float)((double)shift * s / (1.0 + ((double)shift - 1.0) * s));
+  }
+  return DIT_OK;
+}
+
+dit_status dit_linear(int32_t epilogue, const void* a, int64_t lda, const void* w, int64_t ldw,
+                      int32_t M, int32_t N, int32_t K, void* out, int64_t ldo,
+                      const float* bias_or_gate, void* stream) {
+  if (epilogue < DIT_EPI_BF16 || epilogue > DIT_EPI_SWIGLU) return DIT_EINVAL;
+  if (!a || !w || !out || M <= 0 || N <= 0 || K <= 0) return DIT_EINVAL;
+  if (K % 8 || lda < K || ldw < K || lda % 8 || ldw % 8) return DIT_EINVAL;
+  if (!aligned16(a) || !aligned16(w) || !aligned16(out)) return DIT_EINVAL;
+  if (bias_or_gate && !aligned16(bias_or_gate)) return DIT_EINVAL;
+  const bool f32_out = epilogue == DIT_EPI_F32_BIAS || epilogue == DIT_EPI_RESIDUAL;
+  if (ldo < N || ldo % (f32_out ? 4 : 8)) return DIT_EINVAL;
+  if (epilogue == DIT_EPI_SWIGLU && N % 128) return DIT_EUNSUPPORTED;
+  if (!device_state()) return DIT_ECUDA;
+  GemmParams p{};
+  p.M = M;
+  p.N = N;
+  p.K = K;
+  p.out = out;
+  p.ldo = ldo;
+  p.vec = epilogue == DIT_EPI_SWIGLU ? nullptr : bias_or_gate;
+  return cuda_status(launch_gemm(epilogue, 0, a, lda, w, ldw, p, static_cast<cudaStream_t>(stream)));
+}
+
+dit_status dit_qkv_rope(const dit_block_config* cfg, const dit_block_weights* w, const void* a,
+                        int32_t n_tokens, int32_t n_seqs, const float* rope_cos,
+                        const float* rope_sin, void* qk, void* vt, void* stream) {
+  dit_status s = check_block_config(cfg);
+  if (s != DIT_OK) return s;
+  if (!w || !w->w_qkv || !aligned16(w->w_qkv)) return DIT_EINVAL;
+  if (cfg->qk_norm && (!w->q_g || !w->q_b || !w->k_g || !w->k_b)) return DIT_EINVAL;
+  if (!a || !qk || !vt || !rope_cos || !rope_sin || n_tokens <= 0 || n_seqs <= 0 ||
+      n_tokens % n_seqs)
+    return DIT_EINVAL;
+  if (!aligned16(a) || !aligned16(qk) || !aligned16(vt) || !aligned16(rope_cos) ||
+      !aligned16(rope_sin))
+    return DIT_EINVAL;
+  if (!device_state()) return DIT_ECUDA;
+  return run_qkv(cfg, w, a, n_tokens, n_seqs, rope_cos, rope_sin,
+                 static_cast<__nv_bfloat16*>(qk), static_cast<__nv_bfloat16*>(vt),
+                 static_cast<cudaStream_t>(stream));
+}
+
+dit_status dit_attention(const dit_block_config* cfg, const void* qk, const void* vt,
+                         int32_t n_tokens, int32_t n_seqs, void* o, void* stream) {
+  dit_status s = check_block_config(cfg);
+  if (s != DIT_OK) return s;
+  if (!qk || !vt || !o || n_tokens <= 0 || n_seqs <= 0 || n_tokens % n_seqs) return DIT_EINVAL;
+  if (!aligned16(qk) || !aligned16(vt) || !aligned16(o)) return DIT_EINVAL;
+  if (!device_state()) return DIT_ECUDA;
+  return cuda_status(launch_attention(cfg->head_dim, static_cast<const __nv_bfloat16*>(qk),
+                                      static_cast<const __nv_bfloat16*>(vt), n_tokens, n_seqs,
+                                      cfg->n_heads, cfg->n_kv_heads,
+                                      static_cast<__nv_bfloat16*>(o),
+                                      static_cast<cudaStream_t>(stream)));
+}
+
+dit_status dit_ln_modulate(int32_t mode, const float* x, int64_t ldx, int32_t rows, int32_t H,
+                           const float* p0, const float* p1, float eps, void* out, void* stream) {
+  if ((mode != 0 && mode != 1) || !x || !p0 || !p1 || !out || rows < 0 || H <= 0) return DIT_EINVAL;
+  if (H % 4 || ldx < H || ldx % 4) return DIT_EINVAL;
+  if (H > 8192) return DIT_EUNSUPPORTED;
+  if (!aligned16(x) || !aligned16(p0) || !aligned16(p1) || !aligned16(out)) return DIT_EINVAL;
+  return cuda_status(launch_ln_modulate(mode, x, ldx, rows, H, p0, p1, eps,
+                                        static_cast<__nv_bfloat16*>(out), H,
+                                        static_cast<cudaStream_t>(stream)));
+}
+
+dit_status dit_timestep_conditioning(const dit_model_config* cfg, const dit_model_weights* w,
+                                     float sigma, float* mod, float* fin, float* scratch,
+                                     void* stream) {
+  dit_status s = check_model(cfg);
+  if (s != DIT_OK) return s;
+  if (!w || !w->t_w1 || !w->t_w2 || !w->mod_w || !w->fin_w || !mod || !fin || !scratch)
+    return DIT_EINVAL;
+  if (!device_state()) return DIT_ECUDA;
+  return conditioning_impl(cfg, w, sigma, mod, fin, scratch, static_cast<cudaStream_t>(stream));
+}
+
+dit_status dit_rope_table_grid(int32_t grid_h, int32_t grid_w, int32_t n_txt,
+                               const int32_t* rope_axes, float theta, float* cos_out,
+                               float* sin_out, void* stream) {
+  if (grid_h < 0 || grid_w < 0 || n_txt < 0 || !rope_axes || !cos_out || !sin_out)
+    return DIT_EINVAL;
+  if (rope_axes[0] % 2 || rope_axes[1] % 2 || rope_axes[2] % 2) return DIT_EINVAL;
+  if (!device_state()) return DIT_ECUDA;
+  const int half = (rope_axes[0] + rope_axes[1] + rope_axes[2]) / 2;
+  return cuda_status(launch_rope_grid(grid_h, grid_w, n_txt, nullptr, 0, rope_axes, theta, half,
+                                      cos_out, sin_out, static_cast<cudaStream_t>(stream)));
+}
+
+dit_status dit_rope_table_pos(const int32_t* pos, int32_t n, const int32_t* rope_axes, float theta,
+                              float* cos_out, float* sin_out, void* stream) {
+  if (!pos || n < 0 || !rope_axes || !cos_out || !sin_out) return DIT_EINVAL;
+  if (rope_axes[0] % 2 || rope_axes[1] % 2 || rope_axes[2] % 2) return DIT_EINVAL;
+  if (!device_state()) return DIT_ECUDA;
+  const int half = (rope_axes[0] + rope_axes[1] + rope_axes[2]) / 2;
+  return cuda_status(launch_rope_grid(0, 1, 0, pos, n, rope_axes, theta, half, cos_out, sin_out,
+                                      static_cast<cudaStream_t>(stream)));
+}
+
+dit_status dit_rope_table_vit(int32_t grid_h, int32_t grid_w, int32_t n_prefix, int32_t head_dim,
+                              float base, float* cos_out, float* sin_out, void* stream) {
+  if (grid_h < 0 || grid_w < 0 || n_prefix < 0 || head_dim <= 0 || head_dim % 4 || !cos_out ||
+      !sin_out || !(base > 0.0f))
+    return DIT_EINVAL;
+  if (!device_state()) return DIT_ECUDA;
+  return cuda_status(launch_rope_vit(grid_h, grid_w, n_prefix, head_dim, base, cos_out, sin_out,
+                                     static_cast<cudaStream_t>(stream)));
+}
+
+dit_status dit_last_device_error(void* stream) {
+  const DeviceState* ds = device_state();
+  if (!ds) return DIT_ECUDA;
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return DIT_ECUDA;
+  int word = 0;
+  if (cudaMemcpy(&word, ds->err, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return DIT_ECUDA;
+  const int zero = 0;
+  if (cudaMemcpy(ds->err, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess)
+    return DIT_ECUDA;
+  return word ? DIT_ETIMEOUT : DIT_OK;
+}
+
+dit_status dit_set_wait_timeout_ns(uint64_t ns) {
+  const DeviceState* ds = device_state();
+  if (!ds || ns == 0) return ds ? DIT_EINVAL : DIT_ECUDA;
+  std::lock_guard<std::mutex> lock(g_mu);
+  int dev = 0;
+  cudaGetDevice(&dev);
+  g_states[dev].timeout_ns = ns;
+  return DIT_OK;
+}
+
+dit_status dit_debug_stuck_wait(void* stream) {
+  const DeviceState* ds = device_state();
+  if (!ds) return DIT_ECUDA;
+  return cuda_status(launch_stuck_wait(dev_err(ds), static_cast<cudaStream_t>(stream)));
+}
+
+int64_t dit_launch_count(int32_t reset) {
+  const int64_t v = t_launches;
+  if (reset) t_launches = 0;
+  return v;
+}
+
+const char* dit_status_string(dit_status s) {
+  switch (s) {
+    case DIT_OK: return "ok";
+    case DIT_EINVAL: return "invalid argument";
+    case DIT_EUNSUPPORTED: return "shape outside the kernel set";
+    case DIT_EWORKSPACE: return "workspace too small";
+    case DIT_ECUDA: return "CUDA error";
+    case DIT_ETIMEOUT: return "a bounded device wait ran out";
+  }
+  return "unknown status";
+}
+
+}  // extern "C"

@@ -1,0 +1,89 @@
+// Host-side declarations shared by the translation units of libdit.so.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "common.cuh"
+#include "dit.h"
+
+namespace dit {
+
+// Per-device state, initialised on first use with that device current.
+struct DeviceState {
+  int sm_count;
+  int* err;                        // device error word (a __device__ variable)
+  unsigned long long timeout_ns;   // bound of every in-kernel wait
+};
+const DeviceState* device_state();  // nullptr if CUDA is unusable
+inline DevErr dev_err(const DeviceState* ds) { return DevErr{ds->err, ds->timeout_ns}; }
+void count_launch(int n = 1);
+
+// Encodes a row-major bf16 tensor map with 128-byte swizzle.
+// dims[0] is the contiguous dimension; strides_bytes has rank-1 entries.
+bool make_tmap_bf16(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
+                    const uint64_t* strides_bytes, const uint32_t* box);
+
+// ------------------------------------------------------------------ GEMM
+enum GemmEpi : int {
+  EPI_BF16 = 0,       // out bf16 = acc
+  EPI_F32_BIAS = 1,   // out fp32 = acc + bias
+  EPI_RESIDUAL = 2,   // out fp32 += gate * acc
+  EPI_SWIGLU = 3,     // out bf16 = silu(acc_gate) * acc_up
+  EPI_QKV = 4         // qk-LayerNorm + RoPE -> qk buffer; v -> transposed buffer
+};
+
+struct QkvEpi {
+  __nv_bfloat16* qk;   // [M, (nh + nkv) hd]
+  int ldqk;
+  __nv_bfloat16* vt;   // [n_seqs, nkv, hd, s_pad]
+  int s_len, s_pad;
+  int nh, nkv;
+  const float *qg, *qb, *kg, *kb;   // null when there is no qk norm
+  const float *rcos, *rsin;         // [s_len, hd/2]
+  int rope_half;                    // 0: pairs (2k, 2k+1); 1: pairs (k, k + hd/2)
+  float eps;
+};
+
+struct GemmParams {
+  int M, N, K;          // output columns N (SwiGLU: F, the h width)
+  int num_m, num_n;
+  void* out;
+  long long ldo;
+  const float* vec;     // bias (EPI_F32_BIAS) or gate (EPI_RESIDUAL), may be null
+  QkvEpi qkv;
+  DevErr err;
+};
+
+// D = A[M,K] B[rows,K]^T with the epilogue `epi`; hd selects the QKV head
+// width (64 or 128).  Returns cudaSuccess or the launch error.
+cudaError_t launch_gemm(int epi, int hd, const void* A, long long lda, const void* B,
+                        long long ldb, GemmParams& p, cudaStream_t st);
+
+// ------------------------------------------------------------- attention
+cudaError_t launch_attention(int hd, const __nv_bfloat16* qk, const __nv_bfloat16* vt,
+                             int n_tokens, int n_seqs, int nh, int nkv, __nv_bfloat16* o,
+                             cudaStream_t st);
+
+// ------------------------------------------------------------- row ops
+cudaError_t launch_ln_modulate(int mode, const float* x, long long ldx, int rows, int H,
+                               const float* p0, const float* p1, float eps,
+                               __nv_bfloat16* out, long long ldo, cudaStream_t st);
+cudaError_t launch_euler(float* x, const float* v, long long n, float dt, cudaStream_t st);
+cudaError_t launch_gemv(const __nv_bfloat16* W, const float* x, const float* b, float* y,
+                        int O, int K, int silu_in, cudaStream_t st);
+cudaError_t launch_sinusoid(float T, int dim, float* out, cudaStream_t st);
+cudaError_t launch_rope_grid(int grid_h, int grid_w, int n_txt, const int* pos,
+                             int n_pos, const int32_t* axes, float theta, int half_d,
+                             float* cos_out, float* sin_out, cudaStream_t st);
+cudaError_t launch_rope_vit(int grid_h, int grid_w, int n_prefix, int head_dim, float base,
+                            float* cos_out, float* sin_out, cudaStream_t st);
+cudaError_t launch_f32_to_bf16(const float* in, __nv_bfloat16* out, long long n,
+                               cudaStream_t st);
+cudaError_t launch_bf16_to_f32(const __nv_bfloat16* in, float* out, long long n,
+                               cudaStream_t st);
+cudaError_t launch_stuck_wait(DevErr e, cudaStream_t st);
+
+}  // namespace dit

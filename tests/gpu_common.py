@@ -1,0 +1,58 @@
+"""Helpers shared by the GPU parity tests: device transfer, the parity
+criteria, and oracle-side references built only from oracle functions."""
+import numpy as np
+import torch
+
+from diffusion_transformer_image_gb300 import synth
+from oracle import dit_oracle as O
+
+F32 = np.float32
+
+
+def dev():
+    return torch.device("cuda:0")
+
+
+def npf(t: torch.Tensor) -> np.ndarray:
+    return t.detach().to("cpu", torch.float32).numpy()
+
+
+def bf16_normal(shape, name, seed=7, std=1.0, mean=0.0) -> torch.Tensor:
+    """Seeded bf16 CPU tensor (the oracle sees the same values widened)."""
+    return synth.normal(shape, name, seed, std, mean).to(torch.bfloat16)
+
+
+def max_err_vs_rms(got: np.ndarray, ref: np.ndarray):
+    d = np.abs(got.astype(np.float64) - ref.astype(np.float64))
+    rms = float(np.sqrt(np.mean(ref.astype(np.float64) ** 2)))
+    return float(d.max()), rms
+
+
+def assert_block_parity(got, ref, frac=2e-2, what=""):
+    """The per-block criterion: max|err| <= frac * RMS(reference output)."""
+    assert np.isfinite(got).all(), f"{what}: non-finite output"
+    err, rms = max_err_vs_rms(got, ref)
+    assert err <= frac * rms, f"{what}: max|err| {err:.4e} > {frac} x RMS {rms:.4e}"
+    return err / rms
+
+
+def cosine(a, b):
+    a = a.astype(np.float64).ravel()
+    b = b.astype(np.float64).ravel()
+    return float(a @ b / (np.linalg.norm(a) * np.linalg.norm(b)))
+
+
+def oracle_block_config(wl):
+    return O.BlockConfig(wl.hidden, wl.n_heads, wl.n_kv_heads, wl.head_dim, wl.ffn,
+                         rope_layout=wl.rope_layout, adaln=wl.adaln, qk_norm=wl.qk_norm)
+
+
+def oracle_weights(w: dict) -> dict:
+    return {k: synth.to_numpy_f32(v) for k, v in w.items()}
+
+
+def oracle_angles(wl):
+    if wl.rope_layout == "half":
+        return O.rope_angles_vit(wl.grid_h, wl.grid_w, wl.n_prefix, wl.head_dim)
+    return O.rope_angles_3d(O.position_ids(wl.grid_h, wl.grid_w, wl.n_txt), wl.rope_axes,
+                            wl.rope_theta)

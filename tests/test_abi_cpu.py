@@ -1,0 +1,79 @@
+"""CPU checks of the C ABI: the library loads, exports every entry point its
+header declares, and rejects bad arguments on the host without touching a
+GPU.  Builds libdit.so first when it is missing (nvcc cross-compiles)."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "dit.h")
+
+
+@pytest.fixture(scope="module")
+def dit():
+    from diffusion_transformer_image_gb300 import build
+    if not os.path.exists(build.LIB):
+        build.build()
+    from diffusion_transformer_image_gb300 import dit as d
+    return d
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][\w]*\s*\**\s+\**([a-z_][a-z0-9_]*)\s*\(",
+                       src, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_path():
+    names = declared_functions()
+    for n in ("dit_block_forward", "dit_denoise_step", "flowmatch_euler_step"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(dit):
+    names = declared_functions()
+    assert len(names) >= 15
+    for n in names:
+        assert hasattr(dit.lib, n), n
+    assert sorted(dit.EXPORTED) == names
+
+
+def test_sigmas_on_host_match_oracle(dit):
+    from oracle import dit_oracle as O
+    np.testing.assert_array_equal(np.array(dit.flowmatch_sigmas(8, 4.0), np.float32),
+                                  O.flowmatch_sigmas(8, 4.0))
+    np.testing.assert_array_equal(np.array(dit.flowmatch_sigmas(3, 1.0), np.float32),
+                                  O.flowmatch_sigmas(3, 1.0))
+
+
+def test_host_argument_checks(dit):
+    cfg = dit.block_config(4096, 32, 32, 128, 12288)
+    assert dit.lib.dit_block_forward(None, None, None, 0, 1, None, None, None, None, 0, None) == dit.DIT_EINVAL
+    bad = dit.block_config(4096, 32, 32, 96, 12288)
+    assert dit.lib.dit_block_workspace_bytes(ctypes.byref(bad), 4352, 1) == 0
+    gqa_bad = dit.block_config(4096, 32, 5, 128, 12288)
+    assert dit.lib.dit_block_forward(ctypes.byref(gqa_bad), None, None, 1, 1, None, None, None,
+                                     None, 0, None) == dit.DIT_EUNSUPPORTED
+    assert dit.lib.flowmatch_euler_step(ctypes.c_void_p(8), ctypes.c_void_p(16), 16, 1.0, 0.5,
+                                        None) == dit.DIT_EINVAL   # misaligned x
+    assert dit.lib.flowmatch_sigmas(0, 4.0, None) == dit.DIT_EINVAL
+    assert dit.lib.dit_linear(7, None, 0, None, 0, 1, 1, 1, None, 0, None, None) == dit.DIT_EINVAL
+
+
+def test_workspace_sizes(dit):
+    cfg = dit.block_config(4096, 32, 32, 128, 12288)
+    n = 4352
+    ws = dit.lib.dit_block_workspace_bytes(ctypes.byref(cfg), n, 1)
+    # a, o: n x 4096 bf16; qk: n x 8192 bf16; vt: 32 x 128 x n bf16; h: n x 12288 bf16
+    expect = 2 * n * (4096 + 8192 + 4096 + 4096 + 12288)
+    assert expect <= ws <= expect + 5 * 256
+    from diffusion_transformer_image_gb300 import synth
+    m = dit.model_config_from(synth.WORKLOADS["ernie_full"])
+    assert dit.lib.dit_denoise_workspace_bytes(ctypes.byref(m), 64, 64, 256) > ws
+    m.rope_axes[0] = 30   # axes no longer sum to head_dim
+    assert dit.lib.dit_denoise_workspace_bytes(ctypes.byref(m), 64, 64, 256) == 0

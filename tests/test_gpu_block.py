@@ -1,0 +1,226 @@
+"""Block and denoise-step parity on the GPU against the oracle.
+
+Per-block criterion: max|err| <= 2e-2 x RMS(oracle output).  Small cases are
+compared element by element on every output; the full-size workloads are
+compared on sampled rows that the oracle computes one by one (keys and
+values from every row, everything after attention per row)."""
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from diffusion_transformer_image_gb300 import synth
+from gpu_common import (assert_block_parity, cosine, dev, npf, oracle_angles,
+                        oracle_block_config, oracle_weights)
+from oracle import dit_oracle as O
+
+pytestmark = pytest.mark.gpu
+
+dit = pytest.importorskip("diffusion_transformer_image_gb300.dit")
+
+
+def small(name, **kw):
+    return synth.Workload(name, **kw)
+
+
+SMALL_BLOCKS = {
+    "tiny_block": synth.WORKLOADS["tiny_block"],
+    "gqa_small": small("gqa_small", hidden=512, n_heads=4, n_kv_heads=2, head_dim=128, ffn=1024,
+                       grid_h=12, grid_w=12, n_txt=16),
+    "vit_small": small("vit_small", hidden=256, n_heads=4, n_kv_heads=4, head_dim=64, ffn=512,
+                       rope_axes=(), rope_layout="half", adaln=False, qk_norm=False, grid_h=8,
+                       grid_w=8, n_txt=0, n_seqs=2, n_prefix=5),
+}
+
+
+def rope_tables(wl):
+    half = wl.head_dim // 2
+    c = torch.empty(wl.seq_len, half, device=dev())
+    s = torch.empty(wl.seq_len, half, device=dev())
+    if wl.rope_layout == "half":
+        dit.dit_rope_table_vit(wl.grid_h, wl.grid_w, wl.n_prefix, wl.head_dim, 10000.0, c, s)
+    else:
+        dit.dit_rope_table_grid(wl.grid_h, wl.grid_w, wl.n_txt, wl.rope_axes, wl.rope_theta, c, s)
+    return c, s
+
+
+def run_block_gpu(wl, w, x, mod):
+    cfg = dit.block_config_from(wl)
+    blk = dit.DeviceBlock(w, dev())
+    rc, rs = rope_tables(wl)
+    xg = x.to(dev()).contiguous()
+    dit.dit_block_forward(cfg, blk, xg, None if mod is None else mod.to(dev()), rc, rs,
+                          n_seqs=wl.n_seqs)
+    torch.cuda.synchronize()
+    assert dit.dit_last_device_error() == dit.DIT_OK
+    return npf(xg)
+
+
+@pytest.mark.parametrize("name", list(SMALL_BLOCKS))
+def test_block_forward_small(name):
+    wl = SMALL_BLOCKS[name]
+    w = synth.block_weights(wl, 0, seed=0)
+    x = synth.residual_input(wl, seed=1)
+    mod = synth.modulation_input(wl, seed=1) if wl.adaln else None
+    got = run_block_gpu(wl, w, x, mod)
+    ref = O.block_forward(oracle_block_config(wl), oracle_weights(w), npf(x),
+                          None if mod is None else npf(mod), oracle_angles(wl), wl.n_seqs)
+    assert_block_parity(got, ref, what=name)
+
+
+def test_block_zero_gates_pass_through_exactly():
+    wl = synth.WORKLOADS["tiny_block"]
+    w = synth.block_weights(wl, 0, seed=0)
+    x = synth.residual_input(wl, seed=1)
+    mod = synth.modulation_input(wl, seed=1)
+    mod[2] = 0.0
+    mod[5] = 0.0
+    got = run_block_gpu(wl, w, x, mod)
+    np.testing.assert_array_equal(got, npf(x))
+
+
+def test_block_token_permutation_equivariance():
+    # Non-causal attention with position-only RoPE: permuting rows together
+    # with their positions permutes the output.
+    wl = synth.WORKLOADS["tiny_block"]
+    w = synth.block_weights(wl, 0, seed=0)
+    x = synth.residual_input(wl, seed=1)
+    mod = synth.modulation_input(wl, seed=1).to(dev())
+    cfg = dit.block_config_from(wl)
+    blk = dit.DeviceBlock(w, dev())
+    pos = torch.from_numpy(O.position_ids(wl.grid_h, wl.grid_w, wl.n_txt))
+    perm = torch.randperm(wl.n_tokens, generator=torch.Generator().manual_seed(3))
+    outs = []
+    for p in (torch.arange(wl.n_tokens), perm):
+        c = torch.empty(wl.n_tokens, wl.head_dim // 2, device=dev())
+        s = torch.empty_like(c)
+        dit.dit_rope_table_pos(pos[p].contiguous().to(dev()), wl.rope_axes, wl.rope_theta, c, s)
+        xg = x[p].contiguous().to(dev())
+        dit.dit_block_forward(cfg, blk, xg, mod, c, s)
+        outs.append(npf(xg))
+    assert_block_parity(outs[1], outs[0][perm.numpy()], frac=1e-2, what="permutation")
+
+
+def full_block_inputs(wl):
+    w = synth.block_weights(wl, 0, seed=0)
+    x = synth.residual_input(wl, seed=1)
+    mod = synth.modulation_input(wl, seed=1) if wl.adaln else None
+    return w, x, mod
+
+
+@pytest.mark.parametrize("name", ["ernie_block", "krea_gqa"])
+def test_block_forward_full_size_sampled_rows(name):
+    """The 4352-token ERNIE-shaped block and the 1280-token Krea-shaped GQA
+    block at full size, in the launch configuration the bench uses; the
+    oracle computes 48 sampled rows (image, text and tile-edge rows)."""
+    wl = synth.WORKLOADS[name]
+    w, x, mod = full_block_inputs(wl)
+    got = run_block_gpu(wl, w, x, mod)
+    n = wl.n_tokens
+    rng = np.random.default_rng(11)
+    rows = np.unique(np.concatenate([[0, 127, 128, n - 257, n - 256, n - 1],
+                                     rng.choice(n, 42, replace=False)]))
+    ref = O.block_forward_rows(oracle_block_config(wl), oracle_weights(w), npf(x), npf(mod),
+                               oracle_angles(wl), rows)
+    assert_block_parity(got[rows], ref, what=name)
+
+
+def test_vit_block_full_size():
+    """The pre-norm ViT block at full size: 4 images x (5 + 32x32) tokens."""
+    wl = synth.WORKLOADS["vit_backbone"]
+    w, x, _ = full_block_inputs(wl)
+    got = run_block_gpu(wl, w, x, None)
+    ref = O.block_forward(oracle_block_config(wl), oracle_weights(w), npf(x), None,
+                          oracle_angles(wl), wl.n_seqs)
+    assert_block_parity(got, ref, what="vit_backbone")
+
+
+# ------------------------------------------------------------ denoise step
+def oracle_model_config(wl, n_layers):
+    return O.ModelConfig(block=oracle_block_config(wl), n_layers=n_layers,
+                         latent_channels=wl.latent_channels, t_dim=wl.t_dim,
+                         rope_axes=wl.rope_axes, rope_theta=wl.rope_theta)
+
+
+def oracle_model_weights(mw):
+    out = {k: synth.to_numpy_f32(v) for k, v in mw.items() if k != "layers"}
+    out["layers"] = [oracle_weights(l) for l in mw["layers"]]
+    return out
+
+
+def run_denoise(wl, n_layers, sigma, sigma_next):
+    mw = synth.model_weights(wl, seed=0, n_layers=n_layers)
+    latent = synth.latent_input(wl, seed=1)
+    text = synth.text_input(wl, seed=1)
+    cfg = dit.model_config_from(wl, n_layers)
+    model = dit.DeviceModel(mw, dev())
+    lat = latent.to(dev()).contiguous()
+    v = torch.empty_like(lat)
+    dit.dit_denoise_step(cfg, model, lat, text.to(dev()) if wl.n_txt else None, wl.grid_h,
+                         wl.grid_w, sigma, sigma_next, velocity_out=v)
+    torch.cuda.synchronize()
+    assert dit.dit_last_device_error() == dit.DIT_OK
+    new_ref, v_ref = O.denoise_step(oracle_model_config(wl, n_layers), oracle_model_weights(mw),
+                                    npf(latent), npf(text), wl.grid_h, wl.grid_w, sigma,
+                                    sigma_next, return_velocity=True)
+    return npf(lat), npf(v), new_ref, v_ref, npf(latent)
+
+
+TINY_DIT = small("tiny_dit", hidden=256, n_heads=4, n_kv_heads=4, head_dim=64, ffn=768,
+                 rope_axes=(16, 24, 24), grid_h=8, grid_w=8, n_txt=16, n_layers=2,
+                 latent_channels=32)
+
+
+def test_timestep_conditioning():
+    wl = TINY_DIT
+    mw = synth.model_weights(wl, seed=0, n_layers=0)
+    cfg = dit.model_config_from(wl, 0)
+    model = dit.DeviceModel(mw, dev(), layers=[])
+    H = wl.hidden
+    mod = torch.empty(6 * H, device=dev())
+    fin = torch.empty(2 * H, device=dev())
+    scratch = torch.empty(wl.t_dim + 2 * H, device=dev())
+    s = float(O.flowmatch_sigmas(8, 4.0)[3])
+    dit.dit_timestep_conditioning(cfg, model, s, mod, fin, scratch)
+    rmod, rfin = O.conditioning(oracle_model_weights(dict(mw, layers=[])), s, wl.t_dim, 1000.0)
+    np.testing.assert_allclose(npf(mod), rmod.ravel(), rtol=1e-4, atol=1e-5)
+    np.testing.assert_allclose(npf(fin), rfin.ravel(), rtol=1e-4, atol=1e-5)
+
+
+@pytest.mark.parametrize("step", [0, 5])
+def test_denoise_step_tiny(step):
+    s = O.flowmatch_sigmas(8, 4.0)
+    lat, v, new_ref, v_ref, lat0 = run_denoise(TINY_DIT, 2, float(s[step]), float(s[step + 1]))
+    assert_block_parity(v, v_ref, what="velocity")
+    # latent update: parity of the increment and of the new latent
+    assert_block_parity(lat - lat0, new_ref - lat0, what="latent increment")
+    assert cosine(lat, new_ref) >= 0.999
+
+
+@pytest.mark.parametrize("name", ["ernie_full", "krea_gqa"])
+def test_denoise_step_full_size_two_layers(name):
+    """Full token count and width of the 36-layer ERNIE-shaped and 28-layer
+    Krea-shaped denoisers, with 2 layers so the oracle finishes in seconds:
+    conditioning, patch embedding, sequence assembly, RoPE tables, blocks,
+    final norm, projection and Euler update are all exercised at size."""
+    wl = synth.WORKLOADS[name]
+    s = O.flowmatch_sigmas(8, 4.0)
+    lat, v, new_ref, v_ref, lat0 = run_denoise(wl, 2, float(s[1]), float(s[2]))
+    assert_block_parity(v, v_ref, what=f"{name} velocity")
+    assert cosine(v, v_ref) >= 0.999
+    assert cosine(lat, new_ref) >= 0.999
+
+
+@pytest.mark.skipif(not os.environ.get("DIT_FULL_DEPTH"),
+                    reason="full 36/28-layer oracle step takes minutes; set DIT_FULL_DEPTH=1")
+@pytest.mark.parametrize("name", ["ernie_full", "krea_gqa"])
+def test_denoise_step_full_depth(name):
+    """Cosine >= 0.999 after a full-depth step (36 layers ERNIE-shaped, 28
+    Krea-shaped), the whole-step criterion of the workload."""
+    wl = synth.WORKLOADS[name]
+    s = O.flowmatch_sigmas(8, 4.0)
+    lat, v, new_ref, v_ref, _ = run_denoise(wl, wl.n_layers, float(s[0]), float(s[1]))
+    c = cosine(v, v_ref)
+    print(f"{name}: velocity cosine {c:.6f}, latent cosine {cosine(lat, new_ref):.6f}")
+    assert c >= 0.999
