@@ -1,0 +1,427 @@
+"""Benchmark: one flow-matching Euler denoise step of the 36-layer
+ERNIE-shaped DiT (4096 image + 256 text tokens, hidden 4096, 32 x 128 heads,
+SwiGLU 12288, bf16 storage, fp32 accumulation) per step, on one GB300 per
+rank.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+Prints one JSON line.  `value` is ms per denoise step over the whole job
+(replicas: each rank runs its own denoiser; the time is the maximum over
+ranks, divided by the steps all ranks completed).  The step is the whole hot
+path: timestep conditioning, patch embedding, sequence assembly, RoPE tables,
+36 blocks, final norm + projection, Euler update.  Weights (15.7 GB) stream
+from HBM every step, so the working set is far larger than L2.
+
+--impl reference times the CPU oracle on the host cores on a bounded sample
+of the same workload (one of the 36 layers plus the head and tail, scaled to
+36 layers); it is a deliberately slow reference, not the target.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+WORKLOAD = "ernie_full"
+METRIC = "ms per DiT denoise step @4096 tokens bf16; achieved TFLOP/s vs GB300 peak"
+UNIT = "ms/step"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=10)
+    p.add_argument("--warmup", type=int, default=3)
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    return p.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def workload_flops(wl, n_layers):
+    """Algorithmic FLOPs of one denoise step: dense GEMMs 2MNK and non-causal
+    attention 4 N^2 d per head (no skipped work); GEMVs counted 2 per weight."""
+    n = wl.n_tokens
+    H, nh, nkv, d, F, C = wl.hidden, wl.n_heads, wl.n_kv_heads, wl.head_dim, wl.ffn, wl.latent_channels
+    n_img = wl.grid_h * wl.grid_w
+    per_block = {
+        "qkv": 2.0 * n * H * (nh + 2 * nkv) * d,
+        "attention": 4.0 * n * n * d * nh,
+        "out": 2.0 * n * nh * d * H,
+        "gate_up": 2.0 * n * H * 2 * F,
+        "down": 2.0 * n * F * H,
+    }
+    head_tail = 2.0 * n_img * C * H * 2 + 2.0 * n_img * H * C * 2 + 2.0 * (256 * H + H * H + 8 * H * H)
+    return per_block, n_layers * sum(per_block.values()) + head_tail
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return json.load(f), "measured"
+    return FALLBACK_PEAKS, "fallback"
+
+
+def peak_value(peaks, key):
+    v = peaks.get(key)
+    if isinstance(v, dict):
+        v = v.get("value")
+    return float(v) if v is not None else FALLBACK_PEAKS[key]
+
+
+class ClockSampler:
+    """nvidia-smi clock and throttle-reason samples during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.idx = gpu_index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=10)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax = float(f[2])
+            except ValueError:
+                continue
+            for name, val in zip(names, f[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def traffic_for(kernel_key):
+    """DRAM bytes per launch of a kernel from the committed ncu summary, or
+    None when the kernel source changed since the counters were taken."""
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    if not os.path.exists(path):
+        return None
+    src = os.path.join(ROOT, "diffusion_transformer_image_gb300", "csrc")
+    for line in open(path):
+        f = line.split()
+        if len(f) >= 4 and not line.startswith("#") and f[0] == kernel_key:
+            digest = hashlib.sha256(open(os.path.join(src, f[2]), "rb").read()).hexdigest()[:12]
+            return float(f[1]) if digest == f[3] else None
+    return None
+
+
+# ------------------------------------------------------------- oracle arm
+def cpu_oracle_sample(wl, seed=0):
+    """Times the CPU oracle on one of the 36 layers plus the conditioning,
+    patch embedding and final projection; returns (ms per full step scaled to
+    36 layers, sample description, threads)."""
+    import numpy as np
+    from diffusion_transformer_image_gb300 import synth
+    from oracle import dit_oracle as O
+
+    mw = synth.model_weights(wl, seed=seed, n_layers=1)
+    ow = {k: synth.to_numpy_f32(v) for k, v in mw.items() if k != "layers"}
+    lw = {k: synth.to_numpy_f32(v) for k, v in mw["layers"][0].items()}
+    latent = synth.latent_input(wl, seed=1).numpy()
+    text = synth.text_input(wl, seed=1).float().numpy()
+    bc = O.BlockConfig(wl.hidden, wl.n_heads, wl.n_kv_heads, wl.head_dim, wl.ffn)
+    s = O.flowmatch_sigmas(8, 4.0)
+    t0 = time.perf_counter()
+    mod, fin = O.conditioning(ow, float(s[0]), wl.t_dim, 1000.0)
+    x = np.concatenate([O.linear(latent, ow["patch_w"], ow["patch_b"]), text], 0)
+    ang = O.rope_angles_3d(O.position_ids(wl.grid_h, wl.grid_w, wl.n_txt), wl.rope_axes,
+                           wl.rope_theta)
+    t1 = time.perf_counter()
+    x = O.block_forward(bc, lw, x, mod, ang)
+    t2 = time.perf_counter()
+    v = O.final_layer(x[: wl.grid_h * wl.grid_w], fin, ow["out_w"], ow["out_b"], bc.ln_eps)
+    O.euler_step(latent, v, s[0], s[1])
+    t3 = time.perf_counter()
+    ms = ((t1 - t0) + (t3 - t2) + wl.n_layers * (t2 - t1)) * 1e3
+    sample = (f"1 of {wl.n_layers} layers + conditioning, patch embed, final projection and "
+              f"Euler update at full size, layer time x{wl.n_layers}; {t3 - t0:.1f} s of CPU work")
+    return ms, sample, os.cpu_count()
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    from diffusion_transformer_image_gb300 import synth
+    wl = synth.WORKLOADS[WORKLOAD]
+    times = []
+    for _ in range(max(args.steps, 1)):
+        ms, sample, cores = cpu_oracle_sample(wl)
+        times.append(ms)
+    value = statistics.mean(times)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": UNIT,
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(value, 3), "higher_is_better": False, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": config_block(wl),
+        "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def config_block(wl):
+    return {"workload": (f"{WORKLOAD}: ERNIE-shaped DiT denoise step, {wl.n_layers} layers, "
+                         f"{wl.grid_h}x{wl.grid_w} image + {wl.n_txt} text tokens, hidden "
+                         f"{wl.hidden}, {wl.n_heads}x{wl.head_dim} heads, SwiGLU {wl.ffn}, "
+                         f"latent {wl.grid_h * wl.grid_w}x{wl.latent_channels}, 8-step shift-4 "
+                         f"schedule cycled"),
+            "tokens": wl.n_tokens, "layers": wl.n_layers,
+            "l2": "inputs larger than L2: 15.7 GB of bf16 weights stream from HBM each step",
+            "parallelism": "replicas (one independent denoiser per GPU)"}
+
+
+# --------------------------------------------------------------- our arm
+def stage_breakdown(dit, wl, model, x, mod, rc, rs, reps=6):
+    """Per-kernel device time of one block at the step's shapes, each stage
+    launched through its own C-ABI entry point between CUDA events on the
+    stream the kernels run on."""
+    import torch
+    dev = x.device
+    st = torch.cuda.current_stream()
+    n, H, nh, nkv, d, F = wl.n_tokens, wl.hidden, wl.n_heads, wl.n_kv_heads, wl.head_dim, wl.ffn
+    cfg = dit.block_config_from(wl)
+    blk = model.blocks[0]
+    a = torch.empty(n, H, dtype=torch.bfloat16, device=dev)
+    qk = torch.empty(n, (nh + nkv) * d, dtype=torch.bfloat16, device=dev)
+    vt = torch.empty(1, nkv, d, (n + 7) // 8 * 8, dtype=torch.bfloat16, device=dev)
+    o = torch.empty(n, nh * d, dtype=torch.bfloat16, device=dev)
+    h = torch.empty(n, F, dtype=torch.bfloat16, device=dev)
+    xs = x.clone()
+    stages = [
+        ("ln_modulate", lambda: dit.dit_ln_modulate(0, xs, mod[0], mod[1], 1e-6, a)),
+        ("qkv", lambda: dit.dit_qkv_rope(cfg, blk, a, rc, rs, qk, vt)),
+        ("attention", lambda: dit.dit_attention(cfg, qk, vt, o)),
+        ("out", lambda: dit.dit_linear(dit.DIT_EPI_RESIDUAL, o, blk.t["w_o"], xs, mod[2])),
+        ("ln_modulate", lambda: dit.dit_ln_modulate(0, xs, mod[3], mod[4], 1e-6, a)),
+        ("gate_up", lambda: dit.dit_linear(dit.DIT_EPI_SWIGLU, a, blk.t["w_gu"], h)),
+        ("down", lambda: dit.dit_linear(dit.DIT_EPI_RESIDUAL, h, blk.t["w_down"], xs, mod[5])),
+    ]
+    for _, f in stages:   # warm-up
+        f()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(len(stages) * reps + 1)]
+    k = 0
+    ev[0].record(st)
+    for _ in range(reps):
+        for _, f in stages:
+            f()
+            k += 1
+            ev[k].record(st)
+    torch.cuda.synchronize()
+    tot = {}
+    k = 0
+    for _ in range(reps):
+        for name, _ in stages:
+            k += 1
+            tot[name] = tot.get(name, 0.0) + ev[k - 1].elapsed_time(ev[k])
+    # per-block milliseconds (ln_modulate runs twice per block)
+    return {name: t / reps for name, t in tot.items()}
+
+
+def run_ours(args, rank, world, local):
+    import numpy as np
+    import torch
+
+    from diffusion_transformer_image_gb300 import dit, synth
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as tdist
+        tdist.init_process_group("nccl")
+    wl = synth.WORKLOADS[WORKLOAD]
+    # Seeded random-init weights, drawn on the device (no parity is checked
+    # here; the tests compare the same code path against the oracle).
+    mw = synth.model_weights(wl, seed=0, device=dev, n_layers=0)
+    model = dit.DeviceModel(mw, dev, layers=[
+        dit.DeviceBlock(synth.block_weights(wl, li, seed=0, device=dev), dev)
+        for li in range(wl.n_layers)])
+    latent0 = synth.latent_input(wl, seed=1, device=dev)
+    text = synth.text_input(wl, seed=1, device=dev).contiguous()
+    cfg = dit.model_config_from(wl)
+    ws = dit.workspace(dit.dit_denoise_workspace_bytes(cfg, wl.grid_h, wl.grid_w, wl.n_txt), dev)
+    sig = dit.flowmatch_sigmas(8, 4.0)
+    latent = latent0.clone()
+    stream = torch.cuda.current_stream()
+
+    def step(i):
+        j = i % 8
+        dit.dit_denoise_step(cfg, model, latent, text, wl.grid_h, wl.grid_w, sig[j], sig[j + 1],
+                             ws=ws)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = ClockSampler(local)
+    if rank == 0:
+        clocks.start()
+        time.sleep(0.3)
+    dit.dit_launch_count(reset=True)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for i in range(args.steps):
+        step(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    launches = dit.dit_launch_count(reset=True)
+    clk = clocks.stop() if rank == 0 else None
+    if world > 1:
+        torch.distributed.barrier()
+    elapsed_ms = e0.elapsed_time(e1)
+    status = dit.dit_last_device_error()
+    if status != dit.DIT_OK:
+        raise RuntimeError(f"device error word set during the bench: {status}")
+    if world > 1:
+        t = torch.tensor([elapsed_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+    ms_per_step_rank = elapsed_ms / args.steps
+    value = elapsed_ms / (args.steps * world)
+    per_block, step_flops = workload_flops(wl, wl.n_layers)
+    tflops = step_flops / (ms_per_step_rank * 1e-3) / 1e12
+
+    # ---- end to end through the public API with host buffers
+    lat_host = latent0.cpu().pin_memory()
+    txt_host = text.cpu().pin_memory()
+    out_host = torch.empty_like(lat_host).pin_memory()
+    lat_dev = torch.empty_like(latent0)
+    txt_dev = torch.empty_like(text)
+
+    def e2e_step(i):
+        j = i % 8
+        lat_dev.copy_(lat_host, non_blocking=True)
+        txt_dev.copy_(txt_host, non_blocking=True)
+        dit.dit_denoise_step(cfg, model, lat_dev, txt_dev, wl.grid_h, wl.grid_w, sig[j],
+                             sig[j + 1], ws=ws)
+        out_host.copy_(lat_dev, non_blocking=True)
+        stream.synchronize()
+
+    e2e_step(0)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        e2e_step(i)
+    e2e_ms = (time.perf_counter() - t0) * 1e3 / args.steps
+    h2d = lat_host.numel() * 4 + txt_host.numel() * 2
+    d2h = out_host.numel() * 4
+
+    # ---- per-kernel breakdown and the dominant kernel's roofline
+    mod = torch.empty(6, wl.hidden, device=dev)
+    fin = torch.empty(2, wl.hidden, device=dev)
+    scratch = torch.empty(wl.t_dim + 2 * wl.hidden, device=dev)
+    dit.dit_timestep_conditioning(cfg, model, sig[0], mod, fin, scratch)
+    rc = torch.empty(wl.n_tokens, wl.head_dim // 2, device=dev)
+    rs = torch.empty_like(rc)
+    dit.dit_rope_table_grid(wl.grid_h, wl.grid_w, wl.n_txt, wl.rope_axes, wl.rope_theta, rc, rs)
+    x = torch.randn(wl.n_tokens, wl.hidden, device=dev)
+    stages = stage_breakdown(dit, wl, model, x, mod, rc, rs)
+    peaks, peak_src = load_peaks()
+    tc_peak = peak_value(peaks, "bf16_tflops_sustained")
+    hbm_peak = peak_value(peaks, "hbm_gbs")
+    kernels = {}
+    ln_bytes = 6.0 * wl.n_tokens * wl.hidden
+    for name, ms in stages.items():
+        if name == "ln_modulate":
+            gbs = 2 * ln_bytes / (ms * 1e-3) / 1e9   # two launches per block in `ms`
+            kernels[name] = {"ms_per_block": round(ms, 4), "bound": "hbm",
+                             "achieved": round(gbs, 1), "unit": "GB/s",
+                             "frac": round(gbs / hbm_peak, 3)}
+        else:
+            tf = per_block[name] / (ms * 1e-3) / 1e12
+            kernels[name] = {"ms_per_block": round(ms, 4), "bound": "tensor",
+                             "achieved": round(tf, 1), "unit": "TFLOP/s",
+                             "frac": round(tf / tc_peak, 3)}
+    dom = max((k for k in kernels if k != "ln_modulate"), key=lambda k: kernels[k]["ms_per_block"])
+    traffic_key = {"qkv": "gemm_qkv", "attention": "attention", "out": "gemm_out",
+                   "gate_up": "gemm_gate_up", "down": "gemm_down"}[dom]
+    roof = {"kernel": dom, "bound": "tensor", "achieved": kernels[dom]["achieved"],
+            "peak": tc_peak, "unit": "TFLOP/s", "frac": kernels[dom]["frac"],
+            "traffic": traffic_for(traffic_key),
+            "peak_source": f"{peak_src} bf16_tflops_sustained",
+            "algorithmic": f"{per_block[dom]:.4e} FLOP per launch"}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        ms_cpu, sample, cores = cpu_oracle_sample(wl)
+        cpu = {"value": round(ms_cpu, 1), "unit": UNIT, "cores": cores, "kind": "oracle",
+               "sample": sample}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(ms_per_step_rank, 4), "higher_is_better": False,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded N(0,0.02) weights, N(0,1) latent and text)",
+            "config": config_block(wl),
+            "tflops": round(tflops, 1),
+            "tc_frac_of_peak": round(tflops / tc_peak, 3),
+            "clocks": clk,
+            "e2e": {"value": round(e2e_ms, 4), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h},
+            "gpu_launches": launches,
+            "roofline": roof,
+            "kernels": kernels,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def main():
+    args = parse()
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        run_ours(args, rank, world, local)
+
+
+if __name__ == "__main__":
+    main()

@@ -221,7 +221,7 @@ dit_status check_block_weights(const dit_block_config* c, const dit_block_weight
 
 struct StepWs {
   float *x, *rcos, *rsin, *cond, *mod, *fin, *v;
-  __nv_bfloat16* lat;
+  __nv_bfloat16 *lat, *lat_lo, *fin_lo;
   void* block;
   size_t block_bytes;
   size_t bytes;
@@ -248,6 +248,8 @@ StepWs step_ws_layout(const dit_model_config* m, int grid_h, int grid_w, int n_t
   w.fin = reinterpret_cast<float*>(take(2 * H * 4));
   w.v = reinterpret_cast<float*>(take(n_img * C * 4));
   w.lat = reinterpret_cast<__nv_bfloat16*>(take(n_img * C * 2));
+  w.lat_lo = reinterpret_cast<__nv_bfloat16*>(take(n_img * C * 2));
+  w.fin_lo = reinterpret_cast<__nv_bfloat16*>(take(n_img * H * 2));
   BlockWs b = block_ws_layout(c, (int)N, 1, nullptr);
   w.block = take(b.bytes);
   w.block_bytes = b.bytes;
@@ -277,18 +279,17 @@ dit_status conditioning_impl(const dit_model_config* m, const dit_model_weights*
   float* h1 = scratch + m->t_dim;
   float* temb = h1 + H;
   const float T = m->t_scale * sigma;
-  cudaError_t r;
-  if ((r = launch_sinusoid(T, m->t_dim, e, st)) != cudaSuccess) return DIT_ECUDA;
-  if ((r = launch_gemv(static_cast<const __nv_bfloat16*>(w->t_w1), e, w->t_b1, h1, H, m->t_dim, 0,
+  if ((launch_sinusoid(T, m->t_dim, e, st)) != cudaSuccess) return DIT_ECUDA;
+  if ((launch_gemv(static_cast<const __nv_bfloat16*>(w->t_w1), e, w->t_b1, h1, H, m->t_dim, 0,
                        st)) != cudaSuccess)
     return DIT_ECUDA;
-  if ((r = launch_gemv(static_cast<const __nv_bfloat16*>(w->t_w2), h1, w->t_b2, temb, H, H, 1,
+  if ((launch_gemv(static_cast<const __nv_bfloat16*>(w->t_w2), h1, w->t_b2, temb, H, H, 1,
                        st)) != cudaSuccess)
     return DIT_ECUDA;
-  if ((r = launch_gemv(static_cast<const __nv_bfloat16*>(w->mod_w), temb, w->mod_b, mod, 6 * H, H,
+  if ((launch_gemv(static_cast<const __nv_bfloat16*>(w->mod_w), temb, w->mod_b, mod, 6 * H, H,
                        1, st)) != cudaSuccess)
     return DIT_ECUDA;
-  if ((r = launch_gemv(static_cast<const __nv_bfloat16*>(w->fin_w), temb, w->fin_b, fin, 2 * H, H,
+  if ((launch_gemv(static_cast<const __nv_bfloat16*>(w->fin_w), temb, w->fin_b, fin, 2 * H, H,
                        1, st)) != cudaSuccess)
     return DIT_ECUDA;
   return DIT_OK;
@@ -367,8 +368,10 @@ dit_status dit_denoise_step(const dit_model_config* cfg, const dit_model_weights
   const int N = n_img + n_txt;
 
   if ((s = conditioning_impl(cfg, w, sigma, ws.mod, ws.fin, ws.cond, st)) != DIT_OK) return s;
-  // x[0:n_img] = latent Wp^T + bp  (latent rounded to bf16 for the tensor core)
-  if (launch_f32_to_bf16(latent, ws.lat, (long long)n_img * C, st) != cudaSuccess) return DIT_ECUDA;
+  // x[0:n_img] = latent Wp^T + bp.  The latent is fp32: it enters the tensor
+  // core as hi + lo bf16 halves, two passes accumulating into x.
+  if (launch_split_bf16(latent, ws.lat, ws.lat_lo, (long long)n_img * C, st) != cudaSuccess)
+    return DIT_ECUDA;
   {
     GemmParams p{};
     p.M = n_img;
@@ -378,6 +381,9 @@ dit_status dit_denoise_step(const dit_model_config* cfg, const dit_model_weights
     p.ldo = H;
     p.vec = w->patch_b;
     if (launch_gemm(EPI_F32_BIAS, 0, ws.lat, C, w->patch_w, C, p, st) != cudaSuccess)
+      return DIT_ECUDA;
+    p.vec = nullptr;
+    if (launch_gemm(EPI_RESIDUAL, 0, ws.lat_lo, C, w->patch_w, C, p, st) != cudaSuccess)
       return DIT_ECUDA;
   }
   // x[n_img:] = text
@@ -393,9 +399,10 @@ dit_status dit_denoise_step(const dit_model_config* cfg, const dit_model_weights
     s = block_forward_impl(c, &w->layers[l], ws.x, N, 1, ws.mod, ws.rcos, ws.rsin, bws, st);
     if (s != DIT_OK) return s;
   }
-  // v = (LN(x_img) (1 + scale_f) + shift_f) Wout^T + bout; fin = [scale, shift]
-  if (launch_ln_modulate(0, ws.x, H, n_img, H, ws.fin + H, ws.fin, c->ln_eps, bws.a, H, st) !=
-      cudaSuccess)
+  // v = (LN(x_img) (1 + scale_f) + shift_f) Wout^T + bout; fin = [scale, shift].
+  // The fp32 norm output enters the tensor core as hi + lo bf16 halves.
+  if (launch_ln_modulate(0, ws.x, H, n_img, H, ws.fin + H, ws.fin, c->ln_eps, bws.a, H, st,
+                         ws.fin_lo) != cudaSuccess)
     return DIT_ECUDA;
   float* v = velocity_out ? velocity_out : ws.v;
   {
@@ -407,6 +414,9 @@ dit_status dit_denoise_step(const dit_model_config* cfg, const dit_model_weights
     p.ldo = C;
     p.vec = w->out_b;
     if (launch_gemm(EPI_F32_BIAS, 0, bws.a, H, w->out_w, H, p, st) != cudaSuccess)
+      return DIT_ECUDA;
+    p.vec = nullptr;
+    if (launch_gemm(EPI_RESIDUAL, 0, ws.fin_lo, H, w->out_w, H, p, st) != cudaSuccess)
       return DIT_ECUDA;
   }
   const float dt = sigma_next - sigma;

@@ -70,7 +70,8 @@ cudaError_t launch_attention(int hd, const __nv_bfloat16* qk, const __nv_bfloat1
 // ------------------------------------------------------------- row ops
 cudaError_t launch_ln_modulate(int mode, const float* x, long long ldx, int rows, int H,
                                const float* p0, const float* p1, float eps,
-                               __nv_bfloat16* out, long long ldo, cudaStream_t st);
+                               __nv_bfloat16* out, long long ldo, cudaStream_t st,
+                               __nv_bfloat16* out_lo = nullptr);
 cudaError_t launch_euler(float* x, const float* v, long long n, float dt, cudaStream_t st);
 cudaError_t launch_gemv(const __nv_bfloat16* W, const float* x, const float* b, float* y,
                         int O, int K, int silu_in, cudaStream_t st);
@@ -82,6 +83,8 @@ cudaError_t launch_rope_vit(int grid_h, int grid_w, int n_prefix, int head_dim, 
                             float* cos_out, float* sin_out, cudaStream_t st);
 cudaError_t launch_f32_to_bf16(const float* in, __nv_bfloat16* out, long long n,
                                cudaStream_t st);
+cudaError_t launch_split_bf16(const float* in, __nv_bfloat16* hi, __nv_bfloat16* lo, long long n,
+                              cudaStream_t st);
 cudaError_t launch_bf16_to_f32(const __nv_bfloat16* in, float* out, long long n,
                                cudaStream_t st);
 cudaError_t launch_stuck_wait(DevErr e, cudaStream_t st);

@@ -30,10 +30,14 @@ __device__ __forceinline__ float block_sum_128(float v, float* red) {
   return (red[0] + red[1]) + (red[2] + red[3]);
 }
 
+// With `out_lo` the result is also kept to about 16 significant bits as the
+// pair hi = bf16(r), lo = bf16(r - hi): two bf16 GEMMs over hi and lo then
+// reproduce an fp32-input linear (used by the fp32 head and tail projections).
 template <int MODE>
 __global__ void __launch_bounds__(LN_THREADS) ln_modulate_kernel(
     const float* __restrict__ x, long long ldx, int rows, int H, const float* __restrict__ p0,
-    const float* __restrict__ p1, float eps, __nv_bfloat16* __restrict__ out, long long ldo) {
+    const float* __restrict__ p1, float eps, __nv_bfloat16* __restrict__ out, long long ldo,
+    __nv_bfloat16* __restrict__ out_lo) {
   __shared__ float red[4];
   const int row = blockIdx.x;
   if (row >= rows) return;
@@ -86,6 +90,14 @@ __global__ void __launch_bounds__(LN_THREADS) ln_modulate_kernel(
       u.x = pack_bf16x2(r.x, r.y);
       u.y = pack_bf16x2(r.z, r.w);
       orow[idx] = u;
+      if (out_lo) {
+        const __nv_bfloat162* hv = reinterpret_cast<const __nv_bfloat162*>(&u);
+        const float2 h0 = __bfloat1622float2(hv[0]), h1 = __bfloat1622float2(hv[1]);
+        uint2 l;
+        l.x = pack_bf16x2(r.x - h0.x, r.y - h0.y);
+        l.y = pack_bf16x2(r.z - h1.x, r.w - h1.y);
+        reinterpret_cast<uint2*>(out_lo + (size_t)row * ldo)[idx] = l;
+      }
     }
   }
 }
@@ -256,6 +268,19 @@ __global__ void f32_to_bf16_kernel(const float* __restrict__ in, __nv_bfloat16* 
   if (t < n && t < (n4 << 2) + 4) out[t] = __float2bfloat16_rn(in[t]);
 }
 
+// hi = bf16(x), lo = bf16(x - hi): x to about 16 significant bits as two
+// bf16 operands.
+__global__ void split_bf16_kernel(const float* __restrict__ in, __nv_bfloat16* __restrict__ hi,
+                                  __nv_bfloat16* __restrict__ lo, long long n) {
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+       i += (long long)gridDim.x * blockDim.x) {
+    const float x = in[i];
+    const __nv_bfloat16 h = __float2bfloat16_rn(x);
+    hi[i] = h;
+    lo[i] = __float2bfloat16_rn(x - __bfloat162float(h));
+  }
+}
+
 __global__ void bf16_to_f32_kernel(const __nv_bfloat16* __restrict__ in, float* __restrict__ out,
                                    long long n) {
   for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n;
@@ -286,14 +311,17 @@ inline int grid_for(long long work, int threads, int sm_count) {
 
 cudaError_t launch_ln_modulate(int mode, const float* x, long long ldx, int rows, int H,
                                const float* p0, const float* p1, float eps,
-                               __nv_bfloat16* out, long long ldo, cudaStream_t st) {
+                               __nv_bfloat16* out, long long ldo, cudaStream_t st,
+                               __nv_bfloat16* out_lo) {
   if (H > LN_THREADS * 4 * LN_MAXV || (H & 3)) return cudaErrorInvalidValue;
   const int grid = rows;
   if (grid == 0) return cudaSuccess;
   if (mode == 0)
-    ln_modulate_kernel<0><<<grid, LN_THREADS, 0, st>>>(x, ldx, rows, H, p0, p1, eps, out, ldo);
+    ln_modulate_kernel<0><<<grid, LN_THREADS, 0, st>>>(x, ldx, rows, H, p0, p1, eps, out, ldo,
+                                                       out_lo);
   else
-    ln_modulate_kernel<1><<<grid, LN_THREADS, 0, st>>>(x, ldx, rows, H, p0, p1, eps, out, ldo);
+    ln_modulate_kernel<1><<<grid, LN_THREADS, 0, st>>>(x, ldx, rows, H, p0, p1, eps, out, ldo,
+                                                       out_lo);
   count_launch();
   return cudaGetLastError();
 }
@@ -367,6 +395,16 @@ cudaError_t launch_f32_to_bf16(const float* in, __nv_bfloat16* out, long long n,
   if (!ds) return cudaErrorInitializationError;
   if (n == 0) return cudaSuccess;
   f32_to_bf16_kernel<<<grid_for((n + 3) / 4, 256, ds->sm_count), 256, 0, st>>>(in, out, n);
+  count_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_split_bf16(const float* in, __nv_bfloat16* hi, __nv_bfloat16* lo, long long n,
+                              cudaStream_t st) {
+  const DeviceState* ds = device_state();
+  if (!ds) return cudaErrorInitializationError;
+  if (n == 0) return cudaSuccess;
+  split_bf16_kernel<<<grid_for(n, 256, ds->sm_count), 256, 0, st>>>(in, hi, lo, n);
   count_launch();
   return cudaGetLastError();
 }

@@ -56,3 +56,24 @@ def oracle_angles(wl):
         return O.rope_angles_vit(wl.grid_h, wl.grid_w, wl.n_prefix, wl.head_dim)
     return O.rope_angles_3d(O.position_ids(wl.grid_h, wl.grid_w, wl.n_txt), wl.rope_axes,
                             wl.rope_theta)
+
+
+def _bf16(x):
+    return torch.from_numpy(np.ascontiguousarray(x, F32)).to(torch.bfloat16).float().numpy()
+
+
+def bf16_storage_rows(cfg, w, x, mod, angles, rows):
+    """The block on sampled rows, evaluated with oracle functions in fp32 but
+    with the intermediates the CUDA path stores in bf16 (the GEMM inputs a,
+    q/k/v, o, a2, h) rounded to bf16.  Used only to size a tolerance: it
+    measures how far bf16 storage alone moves the fp32 result."""
+    shift1, scale1, gate1, shift2, scale2, gate2 = (mod[i] for i in range(6))
+    a = _bf16(O.modulate(O.layer_norm(x, cfg.ln_eps), shift1, scale1))
+    q, k, v = O.qkv_heads(cfg, a, w, angles)
+    q, k, v = _bf16(q), _bf16(k), _bf16(v)
+    o = _bf16(O.attention_rows(q[rows], k, v, cfg.n_heads, cfg.n_kv_heads))
+    xr = O.gated_residual(x[rows], gate1, O.linear(o, w["w_o"]))
+    a2 = _bf16(O.modulate(O.layer_norm(xr, cfg.ln_eps), shift2, scale2))
+    gu = O.linear(a2, w["w_gu"])
+    h = _bf16(O.silu(gu[:, :cfg.ffn]) * gu[:, cfg.ffn:])
+    return O.gated_residual(xr, gate2, O.linear(h, w["w_down"]))

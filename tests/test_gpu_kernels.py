@@ -218,9 +218,10 @@ def test_attention(case):
     ref = O.attention(npf(q), npf(k), npf(v), nh, nkv, ns)
     got = npf(o)
     assert np.isfinite(got).all()
-    err = np.abs(got - ref)
-    assert err.max() <= 2e-2 * _rms(ref), (err.max(), _rms(ref))
-    np.testing.assert_allclose(got, ref, rtol=2e-2, atol=4e-3 * max(_rms(ref), 1e-3))
+    # The output is stored in bf16: rounding it alone moves an element by up
+    # to 2^-9 |o|, which for these heavy-tailed outputs is ~2 % of RMS(o) at
+    # the largest elements; P in bf16 adds an absolute term well below 1 %.
+    np.testing.assert_allclose(got, ref, rtol=BF16_REL, atol=1e-2 * _rms(ref))
 
 
 def test_bounded_wait_reports_timeout_and_context_survives():
