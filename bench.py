@@ -43,6 +43,9 @@ def parse():
     p.add_argument("--warmup", type=int, default=3)
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--profile-stage", default=None,
+                   help="run the seven stages of one ERNIE-shaped block once after a warm-up "
+                        "pass and exit (a small case for ncu captures)")
     return p.parse_args()
 
 
@@ -261,6 +264,32 @@ def stage_breakdown(dit, wl, model, x, mod, rc, rs, reps=6):
     return {name: t / reps for name, t in tot.items()}
 
 
+def run_profile_stage(args):
+    """One ERNIE-shaped block (436 MB of weights), each stage launched twice:
+    capture the second launch of a kernel with `ncu -k regex:<name> -s 1 -c 1`."""
+    import torch
+    from diffusion_transformer_image_gb300 import dit, synth
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    wl = synth.WORKLOADS["ernie_block"]
+    mw = synth.model_weights(wl, seed=0, device=dev, n_layers=0)
+    model = dit.DeviceModel(mw, dev, layers=[dit.DeviceBlock(
+        synth.block_weights(wl, 0, seed=0, device=dev), dev)])
+    cfg = dit.model_config_from(wl, 1)
+    mod = torch.empty(6, wl.hidden, device=dev)
+    fin = torch.empty(2, wl.hidden, device=dev)
+    scratch = torch.empty(wl.t_dim + 2 * wl.hidden, device=dev)
+    dit.dit_timestep_conditioning(cfg, model, 0.5, mod, fin, scratch)
+    rc = torch.empty(wl.n_tokens, wl.head_dim // 2, device=dev)
+    rs = torch.empty_like(rc)
+    dit.dit_rope_table_grid(wl.grid_h, wl.grid_w, wl.n_txt, wl.rope_axes, wl.rope_theta, rc, rs)
+    x = torch.randn(wl.n_tokens, wl.hidden, device=dev)
+    ms = stage_breakdown(dit, wl, model, x, mod, rc, rs, reps=1)
+    torch.cuda.synchronize()
+    assert dit.dit_last_device_error() == dit.DIT_OK
+    print(json.dumps({"profile_stage": args.profile_stage, "ms_per_block": ms}), flush=True)
+
+
 def run_ours(args, rank, world, local):
     import numpy as np
     import torch
@@ -417,7 +446,9 @@ def run_ours(args, rank, world, local):
 def main():
     args = parse()
     rank, world, local = dist_env()
-    if args.impl == "reference":
+    if args.profile_stage:
+        run_profile_stage(args)
+    elif args.impl == "reference":
         run_reference(args, rank, world)
     else:
         run_ours(args, rank, world, local)

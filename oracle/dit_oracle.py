@@ -23,7 +23,8 @@ Readings taken where the pages are silent or disagree (each one is listed in
 the design doc with its reason):
   * every norm is LayerNorm without affine (eps 1e-6); per-head qk-LayerNorm
     has a gain and bias over head_dim;
-  * qk-LayerNorm is applied before RoPE ([ZFLOW] §VI "head norm + RoPE");
+  * qk-LayerNorm is applied before RoPE ([ZFLOW] §VI: the fused per-head norm
+    kernel normalises each head, then rotates it);
   * RoPE pairs are interleaved inside each axis chunk for the DiT, and
     rotate-half (pairs i, i+d/2) for the ViT;
   * the FFN is SwiGLU: silu(gate) * up, gate rows first in the stacked weight;
@@ -160,8 +161,8 @@ def rope_angles_3d(pos: np.ndarray, axes: Sequence[int], theta: float) -> np.nda
 
 def rope_angles_vit(grid_h: int, grid_w: int, n_prefix: int, head_dim: int,
                     base: float = 10000.0) -> np.ndarray:
-    """Angle table for the pre-norm ViT's rotate-half RoPE ([MAKEPAD]:
-    "rotate-half rope from tables").  The pages give no formula; the reading
+    """Angle table for the pre-norm ViT's rotate-half RoPE, which [MAKEPAD]
+    applies from precomputed tables.  The pages give no formula; the reading
     taken: prefix (cls/register) tokens are unrotated (angle 0); patch token
     (r, c) uses pairs k < d/4 with angle r * w_k and pairs d/4 <= k < d/2 with
     angle c * w_(k-d/4), w_k = base^(-k/(d/4)).  Returns float32
@@ -255,7 +256,7 @@ def attention_rows(q_rows: np.ndarray, k: np.ndarray, v: np.ndarray, n_heads: in
 def qkv_heads(cfg: BlockConfig, a: np.ndarray, w: dict, angles: np.ndarray):
     """QKV projection, per-head qk-LayerNorm (gain, bias over head_dim), then
     RoPE on q and k ([ERNIE] §IV per-layer graph; order norm-then-RoPE per
-    [ZFLOW] §VI "head norm + RoPE").  Returns q [N,nh,d], k, v [N,nkv,d]."""
+    [ZFLOW] §VI, the fused per-head norm then rotation).  Returns q [N,nh,d], k, v [N,nkv,d]."""
     nh, nkv, d = cfg.n_heads, cfg.n_kv_heads, cfg.head_dim
     n = a.shape[0]
     qkv = linear(a, w["w_qkv"])
