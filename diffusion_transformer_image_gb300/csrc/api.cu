@@ -309,6 +309,32 @@ dit_status check_model_weights(const dit_model_config* m, const dit_model_weight
   return DIT_OK;
 }
 
+// ------------------------------------------------ conditioning without allocation
+// Scratch of dit_timestep_conditioning_noalloc: the sinusoid, the first MLP
+// layer and the timestep embedding (t_dim + 2 * hidden floats).  It lives in
+// the library image, so every GPU that loads libdit.so holds these 128 KiB
+// until the process exits, and every call on a device shares them.
+constexpr int NOALLOC_COND_MAX_FLOATS = 32768;
+static __device__ __align__(256) float g_noalloc_cond_scratch[NOALLOC_COND_MAX_FLOATS];
+
+// Device address of the static scratch for the current device.  Host code
+// only holds a stand-in for the array's name; the address is asked of the
+// runtime once per device, with that device current.
+float* noalloc_cond_scratch() {
+  static float* addr[MAX_DEVICES] = {};
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= MAX_DEVICES) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (addr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_cond_scratch) != cudaSuccess || p == nullptr)
+      return nullptr;
+    addr[dev] = static_cast<float*>(p);
+  }
+  return addr[dev];
+}
+
 }  // namespace
 }  // namespace dit
 
@@ -513,6 +539,22 @@ dit_status dit_timestep_conditioning(const dit_model_config* cfg, const dit_mode
   if (!w || !w->t_w1 || !w->t_w2 || !w->mod_w || !w->fin_w || !mod || !fin || !scratch)
     return DIT_EINVAL;
   if (!device_state()) return DIT_ECUDA;
+  return conditioning_impl(cfg, w, sigma, mod, fin, scratch, static_cast<cudaStream_t>(stream));
+}
+
+dit_status dit_timestep_conditioning_noalloc(const dit_model_config* cfg,
+                                             const dit_model_weights* w, float sigma, float* mod,
+                                             float* fin, void* stream) {
+  dit_status s = check_model(cfg);
+  if (s != DIT_OK) return s;
+  if ((long long)cfg->t_dim + 2LL * cfg->block.hidden > NOALLOC_COND_MAX_FLOATS)
+    return DIT_EUNSUPPORTED;
+  if (!w || !w->t_w1 || !w->t_w2 || !w->mod_w || !w->fin_w || !mod || !fin) return DIT_EINVAL;
+  if (!device_state()) return DIT_ECUDA;
+  float* scratch = noalloc_cond_scratch();
+  if (!scratch) return DIT_ECUDA;
+  // Every scratch word is written before it is read (sinusoid, then each
+  // MLP layer), so nothing left by an earlier call needs clearing.
   return conditioning_impl(cfg, w, sigma, mod, fin, scratch, static_cast<cudaStream_t>(stream));
 }
 

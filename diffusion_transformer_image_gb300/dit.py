@@ -34,6 +34,7 @@ EXPORTED = [
     "dit_block_workspace_bytes", "dit_block_forward", "dit_denoise_workspace_bytes",
     "dit_denoise_step", "flowmatch_euler_step", "flowmatch_sigmas", "dit_linear",
     "dit_qkv_rope", "dit_attention", "dit_ln_modulate", "dit_timestep_conditioning",
+    "dit_timestep_conditioning_noalloc",
     "dit_rope_table_grid", "dit_rope_table_pos", "dit_rope_table_vit",
     "dit_last_device_error", "dit_set_wait_timeout_ns", "dit_debug_stuck_wait",
     "dit_launch_count", "dit_status_string",
@@ -97,6 +98,8 @@ _sig("dit_ln_modulate", c_int32, [c_int32, c_void_p, c_int64, c_int32, c_int32, 
                                   c_float, c_void_p, c_void_p])
 _sig("dit_timestep_conditioning", c_int32, [_P(ModelConfig), _P(ModelWeights), c_float, c_void_p,
                                             c_void_p, c_void_p, c_void_p])
+_sig("dit_timestep_conditioning_noalloc", c_int32, [_P(ModelConfig), _P(ModelWeights), c_float,
+                                                    c_void_p, c_void_p, c_void_p])
 _sig("dit_rope_table_grid", c_int32, [c_int32, c_int32, c_int32, _P(c_int32), c_float, c_void_p,
                                       c_void_p, c_void_p])
 _sig("dit_rope_table_pos", c_int32, [c_void_p, c_int32, _P(c_int32), c_float, c_void_p, c_void_p,
@@ -269,6 +272,16 @@ def dit_timestep_conditioning(cfg: ModelConfig, w: DeviceModel, sigma: float, mo
     _check(lib.dit_timestep_conditioning(ctypes.byref(cfg), ctypes.byref(w.c), sigma, _ptr(mod),
                                          _ptr(fin), _ptr(scratch), _stream(stream)),
            "dit_timestep_conditioning")
+
+
+def dit_timestep_conditioning_noalloc(cfg: ModelConfig, w: DeviceModel, sigma: float, mod, fin,
+                                      stream=None):
+    """dit_timestep_conditioning without a scratch argument: for callers that
+    may not allocate device memory (the scratch is a static array in the
+    library).  Calls that overlap on the GPU race on that array."""
+    _check(lib.dit_timestep_conditioning_noalloc(ctypes.byref(cfg), ctypes.byref(w.c), sigma,
+                                                 _ptr(mod), _ptr(fin), _stream(stream)),
+           "dit_timestep_conditioning_noalloc")
 
 
 def dit_rope_table_grid(grid_h: int, grid_w: int, n_txt: int, axes: Sequence[int], theta: float,

@@ -190,7 +190,7 @@ dit_status dit_linear(int32_t epilogue, const void* a, int64_t lda, const void* 
                       int64_t ldo, const float* bias_or_gate, void* stream);
 
 /* The QKV projection with its fused epilogue ([ERNIE] section IV; [ZFLOW]
- * section VI, "head norm + RoPE"): [q|k|v] = a Wqkv^T, then per head
+ * section VI, the fused per-head norm then rotation): [q|k|v] = a Wqkv^T, then per head
  * q <- RoPE(LN_d(q) q_g + q_b), k likewise, v unchanged.
  * a: device bf16 [n_tokens, H].  Outputs:
  *   qk: device bf16 [n_tokens, (n_heads + n_kv_heads) d], q heads then k heads
@@ -225,6 +225,33 @@ dit_status dit_timestep_conditioning(const dit_model_config* cfg,
                                      const dit_model_weights* w, float sigma,
                                      float* mod, float* fin, float* scratch,
                                      void* stream);
+
+/* The same timestep conditioning for callers that cannot allocate device
+ * memory: it needs no scratch argument.  No counterpart on the pages; this is
+ * an interface addition of this library.
+ *
+ * Who needs it: code that is handed a stream but may not allocate on it --
+ * a host application or inference server that gives this library a fixed
+ * memory budget and forbids allocations behind its back, or a caller on a
+ * latency-critical path where cudaMalloc/cudaFree would synchronise the
+ * device.  The scratch (t_dim + 2 * hidden floats) is a static array inside
+ * libdit.so of 32768 floats (128 KiB), held on every GPU that loads the
+ * library until the process exits.
+ *
+ * Limits and behaviour:
+ *   - t_dim + 2 * hidden > 32768 returns DIT_EUNSUPPORTED (nothing enqueued).
+ *   - Allocates nothing: no cudaMalloc, cudaFree or allocating library call.
+ *   - The first call on a device asks the runtime for the array's device
+ *     address (once per device, that device current); make that first call
+ *     before any stream capture.
+ *   - All calls on a device share the one array and it keeps the last call's
+ *     contents; every word is written before it is read, so no clearing is
+ *     needed.  Calls that overlap on the GPU (different streams, or
+ *     concurrent host threads) race on it: serialise them.
+ * mod [6H] and fin [2H]: device fp32 outputs, as dit_timestep_conditioning. */
+dit_status dit_timestep_conditioning_noalloc(const dit_model_config* cfg,
+                                             const dit_model_weights* w, float sigma,
+                                             float* mod, float* fin, void* stream);
 
 /* RoPE tables for the joint DiT sequence ([ERNIE] section IV token layout and
  * section VII, Decision 3): token t < grid_h grid_w is image cell
