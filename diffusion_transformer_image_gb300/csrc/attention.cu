@@ -6,8 +6,10 @@
 // CUDA to Pure Rust + Metal 4", section VI, attention(heads, kv_heads)).
 //
 // One CTA computes 128 query rows of one head of one sequence.  Roles:
-//   warp 0      TMA producer: the q tile once, then k and v tiles of 128 keys
-//               through a two-stage ring
+//   warp 0      TMA producer of the q tile and of k tiles of 128 keys (a
+//               two-stage ring released as soon as S_j = q k_j^T completes)
+//   warp 6      TMA producer of v tiles (a two-stage ring released when
+//               O += P_j v_j completes)
 //   warp 1      TMEM allocator and MMA issuer: S_j = q k_j^T into one of two
 //               TMEM score buffers, then O += P_j v_j into the TMEM output
 //   warps 2..5  softmax: thread t owns query row t; reads S_j from TMEM,
@@ -28,7 +30,7 @@ namespace dit {
 namespace {
 
 constexpr int BQ = 128, BKV = 128;
-constexpr int NUM_THREADS = 192;
+constexpr int NUM_THREADS = 224;
 constexpr float RESCALE_LOG2 = 8.0f;
 
 template <int HD>
@@ -48,7 +50,7 @@ struct AttnLayout {
 
 struct AttnBars {
   uint64_t q_full;
-  uint64_t k_full[2], v_full[2], kv_empty[2];
+  uint64_t k_full[2], k_empty[2], v_full[2], v_empty[2];
   uint64_t s_full[2], s_free[2];
   uint64_t p_full[2], pv_done[2];
   uint64_t drain;
@@ -90,8 +92,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     mbar_init(&bars->q_full, 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars->k_full[i], 1);
+      mbar_init(&bars->k_empty[i], 1);
       mbar_init(&bars->v_full[i], 1);
-      mbar_init(&bars->kv_empty[i], 1);
+      mbar_init(&bars->v_empty[i], 1);
       mbar_init(&bars->s_full[i], 1);
       mbar_init(&bars->s_free[i], 4);
       mbar_init(&bars->p_full[i], 4);
@@ -113,7 +116,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   if (warp == 0) {
     if (lane == 0) {
-      // -------------------------------------------------- TMA producer
+      // ---------------------------------------------- TMA producer: q, k
       mbar_arrive_expect_tx(&bars->q_full, L::Q_BYTES);
 #pragma unroll
       for (int pn = 0; pn < HD / 64; ++pn)
@@ -122,14 +125,30 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       for (int j = 0; j < nb; ++j) {
         const int st = j & 1;
         const uint32_t ph = (j >> 1) & 1;
-        if (!mbar_wait(&bars->kv_empty[st], ph ^ 1u, p.err)) break;
+        if (!mbar_wait(&bars->k_empty[st], ph ^ 1u, p.err)) break;
         uint8_t* sk = smem + L::OFF_K + st * L::K_BYTES;
-        uint8_t* sv = smem + L::OFF_V + st * L::V_BYTES;
         mbar_arrive_expect_tx(&bars->k_full[st], L::K_BYTES);
 #pragma unroll
         for (int pn = 0; pn < HD / 64; ++pn)
           tma_load_3d(sk + pn * 16384, &tmQK, &bars->k_full[st], (p.nh + g) * HD + pn * 64,
                       j * BKV, seq);
+        filled |= 1u << st;
+        fill_parity = (fill_parity & ~(1u << st)) | (ph << st);
+      }
+      // every copy issued must land before the CTA may exit
+      mbar_wait(&bars->q_full, 0, p.err);
+      for (int s = 0; s < 2; ++s)
+        if (filled & (1u << s)) mbar_wait(&bars->k_full[s], (fill_parity >> s) & 1u, p.err);
+    }
+  } else if (warp == 6) {
+    if (lane == 0) {
+      // ------------------------------------------------- TMA producer: v
+      uint32_t filled = 0, fill_parity = 0;
+      for (int j = 0; j < nb; ++j) {
+        const int st = j & 1;
+        const uint32_t ph = (j >> 1) & 1;
+        if (!mbar_wait(&bars->v_empty[st], ph ^ 1u, p.err)) break;
+        uint8_t* sv = smem + L::OFF_V + st * L::V_BYTES;
         mbar_arrive_expect_tx(&bars->v_full[st], L::V_BYTES);
 #pragma unroll
         for (int pn = 0; pn < 2; ++pn)
@@ -138,12 +157,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         filled |= 1u << st;
         fill_parity = (fill_parity & ~(1u << st)) | (ph << st);
       }
-      mbar_wait(&bars->q_full, 0, p.err);
       for (int s = 0; s < 2; ++s)
-        if (filled & (1u << s)) {
-          mbar_wait(&bars->k_full[s], (fill_parity >> s) & 1u, p.err);
-          mbar_wait(&bars->v_full[s], (fill_parity >> s) & 1u, p.err);
-        }
+        if (filled & (1u << s)) mbar_wait(&bars->v_full[s], (fill_parity >> s) & 1u, p.err);
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -167,6 +182,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             umma_bf16(s_tmem, sdesc_sw128(q_addr + off), sdesc_sw128(k_addr + off), idesc_s, k > 0);
           }
           umma_commit(&bars->s_full[st]);
+          umma_commit(&bars->k_empty[st]);
         }
         if (j >= 1) {
           const int i = j - 1;
@@ -184,13 +200,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                       (i > 0 || k > 0) ? 1u : 0u);
           }
           umma_commit(&bars->pv_done[pb]);
-          umma_commit(&bars->kv_empty[pb]);
+          umma_commit(&bars->v_empty[pb]);
         }
       }
       umma_commit(&bars->drain);
       mbar_wait(&bars->drain, 0, p.err);
     }
-  } else {
+  } else if (warp >= 2 && warp <= 5) {
     // ---------------------------------------------------- softmax warps
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;  // query row within the tile
@@ -231,7 +247,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       if (__any_sync(0xffffffffu, need) && j > 0) {
         // O holds PV_0 .. PV_{j-1}; wait for the last one, then rescale rows
         // whose maximum moved (alpha = 1 for the others).
-        const float alpha = need ? exp2f(m_used - mx) : 1.0f;
+        const float alpha = need ? ex2_approx(m_used - mx) : 1.0f;
         if (!mbar_wait(&bars->pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, p.err)) {
           ok = false;
           break;
@@ -253,7 +269,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       float rs = 0.f;
 #pragma unroll
       for (int c = 0; c < BKV; ++c) {
-        s[c] = exp2f(fmaf(s[c], p.scale_log2, -m_used));
+        s[c] = ex2_approx(fmaf(s[c], p.scale_log2, -m_used));
         rs += s[c];
       }
       l += rs;
