@@ -229,7 +229,7 @@ def stage_breakdown(dit, wl, model, x, mod, rc, rs, reps=6):
     cfg = dit.block_config_from(wl)
     blk = model.blocks[0]
     a = torch.empty(n, H, dtype=torch.bfloat16, device=dev)
-    qk = torch.empty(n, (nh + nkv) * d, dtype=torch.bfloat16, device=dev)
+    qk = torch.empty(nh + nkv, n, d, dtype=torch.bfloat16, device=dev)
     vt = torch.empty(1, nkv, d, (n + 7) // 8 * 8, dtype=torch.bfloat16, device=dev)
     o = torch.empty(n, nh * d, dtype=torch.bfloat16, device=dev)
     h = torch.empty(n, F, dtype=torch.bfloat16, device=dev)

@@ -134,7 +134,6 @@ dit_status run_qkv(const dit_block_config* c, const dit_block_weights* w, const 
   p.N = (c->n_heads + 2 * c->n_kv_heads) * hd;
   p.K = c->hidden;
   p.qkv.qk = qk;
-  p.qkv.ldqk = (c->n_heads + c->n_kv_heads) * hd;
   p.qkv.vt = vt;
   p.qkv.s_len = n_tokens / n_seqs;
   p.qkv.s_pad = (p.qkv.s_len + 7) & ~7;

@@ -5,22 +5,29 @@
 // grouped KV heads g = h / (n_heads / n_kv_heads) ([ZFLOW] "From Python +
 // CUDA to Pure Rust + Metal 4", section VI, attention(heads, kv_heads)).
 //
-// One CTA computes 128 query rows of one head of one sequence.  Roles:
-//   warp 0      TMA producer of the q tile and of k tiles of 128 keys (a
-//               two-stage ring released as soon as S_j = q k_j^T completes)
-//   warp 6      TMA producer of v tiles (a two-stage ring released when
-//               O += P_j v_j completes)
-//   warp 1      TMEM allocator and MMA issuer: S_j = q k_j^T into one of two
-//               TMEM score buffers, then O += P_j v_j into the TMEM output
-//   warps 2..5  softmax: thread t owns query row t; reads S_j from TMEM,
-//               keeps the running maximum and sum, writes P_j (bf16) to
-//               shared memory in the swizzled layout the tensor core reads,
-//               and rescales O in TMEM when the maximum grows by more than
-//               2^8 (smaller growth is absorbed: exponentials stay <= 256)
-// The issue order S_0, S_1, PV_0, S_2, PV_1, ... lets the softmax of block j
-// overlap the tensor core work on blocks j + 1 and j - 1.
+// One CTA computes two tiles of 128 query rows (A and B) of one head of one
+// sequence, so every k/v tile loaded serves 256 queries: the kernel needs
+// half the shared-memory ingress per FLOP of a one-tile design, which is
+// what bounds a 128 x 128 attention block on this part.  Roles:
+//   warp 0       TMA producer: both q tiles, then k tiles of 128 keys
+//   warp 2       TMA producer: v tiles (transposed, 128 keys)
+//   warp 1       TMEM allocator and MMA issuer, per key block j and tile t:
+//                  O_t += P_t(j) v_j  (P read from TMEM), then
+//                  S_t(j+1) = q_t k_{j+1}^T once that PV has completed,
+//                  since P_t(j) occupies S_t's columns.
+//   warps 3..18  softmax, eight per tile: query row r of tile t is shared by
+//                two warps (the same TMEM lane quarter), each owning 64 of
+//                the 128 scores of a block.  They exchange row maxima through
+//                shared memory, keep the running maximum and their partial
+//                sums, overwrite S_t with P_t (bf16, two per 32-bit column),
+//                and rescale their half of O_t when the maximum grows by more
+//                than 2^8 (smaller growth is absorbed: exponentials stay
+//                <= 256).  While the softmax of one tile runs, the tensor
+//                core works on the other tile.
+// TMEM columns: S_A/P_A [0,128), S_B/P_B [128,256), O_A, O_B after them.
 //
-// v arrives transposed (vt[seq][g][c][key]) so that both MMAs read K-major
+// q and k arrive head-major (qk[head][token][d], so a tile is one contiguous
+// block) and v transposed (vt[seq][g][c][key]) so that both MMAs read K-major
 // operands.
 #include <math_constants.h>
 
@@ -30,46 +37,99 @@ namespace dit {
 namespace {
 
 constexpr int BQ = 128, BKV = 128;
-constexpr int NUM_THREADS = 224;
+constexpr int NUM_THREADS = 19 * 32;
+constexpr int NUM_SOFTMAX_WARPS = 16;   // 8 per query tile
 constexpr float RESCALE_LOG2 = 8.0f;
+
+// Ring depths per head width, sized to 227 KB of shared memory.
+template <int HD>
+struct AttnStages;
+template <>
+struct AttnStages<128> {
+  static constexpr int K = 2, V = 2;
+};
+template <>
+struct AttnStages<64> {
+  static constexpr int K = 5, V = 5;
+};
 
 template <int HD>
 struct AttnLayout {
-  static constexpr int Q_BYTES = BQ * HD * 2;     // HD/64 panels of 128 rows x 128 B
+  static constexpr int KS = AttnStages<HD>::K, VS = AttnStages<HD>::V;
+  static constexpr int Q_BYTES = BQ * HD * 2;     // per tile: HD/64 panels of 128 rows x 128 B
   static constexpr int K_BYTES = BKV * HD * 2;    // HD/64 panels of 128 keys x 128 B
   static constexpr int V_BYTES = HD * BKV * 2;    // 2 panels of HD rows x 64 keys
   static constexpr int V_PANEL = HD * 128;
-  static constexpr int P_BYTES = BQ * BKV * 2;    // 2 panels of 128 rows x 64 keys
-  static constexpr int OFF_Q = 0;
-  static constexpr int OFF_K = OFF_Q + Q_BYTES;
-  static constexpr int OFF_V = OFF_K + 2 * K_BYTES;
-  static constexpr int OFF_P = OFF_V + 2 * V_BYTES;
-  static constexpr int OFF_BAR = OFF_P + 2 * P_BYTES;
-  static constexpr int O_COL = 2 * BKV;           // TMEM columns: S0, S1, then O
+  static constexpr int OFF_Q = 0;                 // tile A, then tile B
+  static constexpr int OFF_K = OFF_Q + 2 * Q_BYTES;
+  static constexpr int OFF_V = OFF_K + KS * K_BYTES;
+  static constexpr int OFF_BAR = OFF_V + VS * V_BYTES;
+  static constexpr int OFF_RED = OFF_BAR + 512;   // [tile][half][128 rows] fp32 exchange
+  static constexpr int END = OFF_RED + 2 * 2 * BQ * 4;
+  static constexpr int O_COL = 2 * BKV;           // O_A, then O_B
+  static_assert(O_COL + 2 * HD <= 512, "TMEM overflow");
 };
+
+constexpr int MAX_STAGES = 6;
 
 struct AttnBars {
   uint64_t q_full;
-  uint64_t k_full[2], k_empty[2], v_full[2], v_empty[2];
-  uint64_t s_full[2], s_free[2];
-  uint64_t p_full[2], pv_done[2];
+  uint64_t k_full[MAX_STAGES], k_empty[MAX_STAGES], v_full[MAX_STAGES], v_empty[MAX_STAGES];
+  uint64_t s_full[2], p_full[2], pv_done[2];   // per query tile
+  uint64_t xchg[2][4];  // per tile and TMEM lane quarter: the two warps of those rows
   uint64_t drain;
   uint32_t tmem_slot;
 };
 
+static_assert(sizeof(AttnBars) <= 512, "barrier block overflows its slot");
+
 template <int HD>
 constexpr size_t attn_smem_bytes() {
-  return (size_t)AttnLayout<HD>::OFF_BAR + sizeof(AttnBars) + 1024 + 64;
+  return (size_t)AttnLayout<HD>::END + 1024;  // + slack to align the base to 1024 B
+}
+
+// The two softmax warps that share a tile's TMEM lane quarter meet here: each
+// arrives once (lane 0, after the warp's shared-memory writes), then waits for
+// the other.  Bounded like every other wait.
+__device__ __forceinline__ bool pair_sync(uint64_t* bar, uint32_t& uses, const DevErr& e) {
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
+  const bool ok = mbar_wait(bar, uses & 1u, e);
+  ++uses;
+  return ok;
 }
 
 struct AttnParams {
   __nv_bfloat16* o;
   int ldo;
-  int s_len;
+  int s_len, n_seqs;
   int nh, nkv;
   float scale_log2;
   DevErr err;
 };
+
+template <int HD>
+__device__ __forceinline__ void issue_s(uint32_t s_tmem, uint32_t q_addr, uint32_t k_addr) {
+  constexpr uint32_t idesc_s = idesc_bf16_f32(BQ, BKV);
+#pragma unroll
+  for (int k = 0; k < HD / 16; ++k) {
+    const uint32_t off = (k >> 2) * 16384 + (k & 3) * 32;
+    umma_bf16(s_tmem, sdesc_sw128(q_addr + off), sdesc_sw128(k_addr + off), idesc_s, k > 0);
+  }
+}
+
+template <int HD>
+__device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem, uint32_t v_addr,
+                                         bool first) {
+  using L = AttnLayout<HD>;
+  constexpr uint32_t idesc_o = idesc_bf16_f32(BQ, HD);
+#pragma unroll
+  for (int k = 0; k < BKV / 16; ++k) {
+    const uint32_t voff = (k >> 2) * L::V_PANEL + (k & 3) * 32;
+    umma_bf16_ts(o_tmem, p_tmem + k * 8, sdesc_sw128(v_addr + voff), idesc_o,
+                 (!first || k > 0) ? 1u : 0u);
+  }
+}
 
 template <int HD>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
@@ -82,23 +142,29 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   AttnBars* bars = reinterpret_cast<AttnBars*>(smem + L::OFF_BAR);
 
   const int warp = warp_id(), lane = lane_id();
-  const int q0 = blockIdx.x * BQ;
+  const int q0 = blockIdx.x * 2 * BQ;
   const int h = blockIdx.y;
   const int seq = blockIdx.z;
   const int g = h / (p.nh / p.nkv);
   const int nb = (p.s_len + BKV - 1) / BKV;
+  // Key blocks are visited starting at a block that depends on the query
+  // tile, so the CTAs of one head stream different k/v tiles at any moment.
+  // Softmax is order-independent; only the rounding order changes.
+  const int kb0 = blockIdx.x % nb;
 
   if (threadIdx.x == 0) {
     mbar_init(&bars->q_full, 1);
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < MAX_STAGES; ++i) {
       mbar_init(&bars->k_full[i], 1);
       mbar_init(&bars->k_empty[i], 1);
       mbar_init(&bars->v_full[i], 1);
       mbar_init(&bars->v_empty[i], 1);
-      mbar_init(&bars->s_full[i], 1);
-      mbar_init(&bars->s_free[i], 4);
-      mbar_init(&bars->p_full[i], 4);
-      mbar_init(&bars->pv_done[i], 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(&bars->s_full[t], 1);
+      mbar_init(&bars->p_full[t], NUM_SOFTMAX_WARPS / 2);
+      mbar_init(&bars->pv_done[t], 1);
+      for (int q = 0; q < 4; ++q) mbar_init(&bars->xchg[t][q], 2);
     }
     mbar_init(&bars->drain, 1);
     fence_barrier_init();
@@ -117,209 +183,221 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   if (warp == 0) {
     if (lane == 0) {
       // ---------------------------------------------- TMA producer: q, k
-      mbar_arrive_expect_tx(&bars->q_full, L::Q_BYTES);
+      mbar_arrive_expect_tx(&bars->q_full, 2 * L::Q_BYTES);
 #pragma unroll
-      for (int pn = 0; pn < HD / 64; ++pn)
-        tma_load_3d(smem + L::OFF_Q + pn * 16384, &tmQK, &bars->q_full, h * HD + pn * 64, q0, seq);
+      for (int t = 0; t < 2; ++t)
+#pragma unroll
+        for (int pn = 0; pn < HD / 64; ++pn)
+          tma_load_2d(smem + L::OFF_Q + t * L::Q_BYTES + pn * 16384, &tmQK, &bars->q_full,
+                      pn * 64, (h * p.n_seqs + seq) * p.s_len + q0 + t * BQ);
       uint32_t filled = 0, fill_parity = 0;
       for (int j = 0; j < nb; ++j) {
-        const int st = j & 1;
-        const uint32_t ph = (j >> 1) & 1;
+        const int st = j % L::KS;
+        const uint32_t ph = (j / L::KS) & 1;
         if (!mbar_wait(&bars->k_empty[st], ph ^ 1u, p.err)) break;
         uint8_t* sk = smem + L::OFF_K + st * L::K_BYTES;
         mbar_arrive_expect_tx(&bars->k_full[st], L::K_BYTES);
 #pragma unroll
         for (int pn = 0; pn < HD / 64; ++pn)
-          tma_load_3d(sk + pn * 16384, &tmQK, &bars->k_full[st], (p.nh + g) * HD + pn * 64,
-                      j * BKV, seq);
+          tma_load_2d(sk + pn * 16384, &tmQK, &bars->k_full[st], pn * 64,
+                      ((p.nh + g) * p.n_seqs + seq) * p.s_len + ((j + kb0) % nb) * BKV);
         filled |= 1u << st;
         fill_parity = (fill_parity & ~(1u << st)) | (ph << st);
       }
       // every copy issued must land before the CTA may exit
       mbar_wait(&bars->q_full, 0, p.err);
-      for (int s = 0; s < 2; ++s)
+      for (int s = 0; s < L::KS; ++s)
         if (filled & (1u << s)) mbar_wait(&bars->k_full[s], (fill_parity >> s) & 1u, p.err);
     }
-  } else if (warp == 6) {
+  } else if (warp == 2) {
     if (lane == 0) {
       // ------------------------------------------------- TMA producer: v
       uint32_t filled = 0, fill_parity = 0;
       for (int j = 0; j < nb; ++j) {
-        const int st = j & 1;
-        const uint32_t ph = (j >> 1) & 1;
+        const int st = j % L::VS;
+        const uint32_t ph = (j / L::VS) & 1;
         if (!mbar_wait(&bars->v_empty[st], ph ^ 1u, p.err)) break;
         uint8_t* sv = smem + L::OFF_V + st * L::V_BYTES;
         mbar_arrive_expect_tx(&bars->v_full[st], L::V_BYTES);
 #pragma unroll
         for (int pn = 0; pn < 2; ++pn)
-          tma_load_3d(sv + pn * L::V_PANEL, &tmV, &bars->v_full[st], j * BKV + pn * 64, g * HD,
-                      seq);
+          tma_load_2d(sv + pn * L::V_PANEL, &tmV, &bars->v_full[st],
+                      ((j + kb0) % nb) * BKV + pn * 64, (seq * p.nkv + g) * HD);
         filled |= 1u << st;
         fill_parity = (fill_parity & ~(1u << st)) | (ph << st);
       }
-      for (int s = 0; s < 2; ++s)
+      for (int s = 0; s < L::VS; ++s)
         if (filled & (1u << s)) mbar_wait(&bars->v_full[s], (fill_parity >> s) & 1u, p.err);
     }
   } else if (warp == 1) {
     if (lane == 0) {
       // -------------------------------------------------- MMA issuer
-      constexpr uint32_t idesc_s = idesc_bf16_f32(BQ, BKV);
-      constexpr uint32_t idesc_o = idesc_bf16_f32(BQ, HD);
       const uint32_t q_addr = smem_u32(smem + L::OFF_Q);
-      const uint32_t o_tmem = tmem_base + L::O_COL;
-      bool ok = mbar_wait(&bars->q_full, 0, p.err);
-      for (int j = 0; j <= nb && ok; ++j) {
-        if (j < nb) {
-          const int st = j & 1;
-          if (!mbar_wait(&bars->k_full[st], (j >> 1) & 1, p.err)) break;
-          if (j >= 2 && !mbar_wait(&bars->s_free[st], ((j - 2) >> 1) & 1, p.err)) break;
-          tc_fence_after();
-          const uint32_t k_addr = smem_u32(smem + L::OFF_K + st * L::K_BYTES);
-          const uint32_t s_tmem = tmem_base + st * BKV;
+      bool ok = mbar_wait(&bars->q_full, 0, p.err) && mbar_wait(&bars->k_full[0], 0, p.err);
+      if (ok) {
+        tc_fence_after();
+        const uint32_t k_addr = smem_u32(smem + L::OFF_K);
+        issue_s<HD>(tmem_base, q_addr, k_addr);
+        umma_commit(&bars->s_full[0]);
+        issue_s<HD>(tmem_base + BKV, q_addr + L::Q_BYTES, k_addr);
+        umma_commit(&bars->s_full[1]);
+        umma_commit(&bars->k_empty[0]);
+      }
+      // Per key block j, tile by tile: O_t += P_t(j) v_j, then (once that
+      // has completed, since P_t(j) occupies S_t's columns) S_t(j+1).  Tile
+      // A's chain never waits on tile B's softmax, so the two softmax groups
+      // alternate on the special-function units while the tensor core works
+      // on the other tile.
+      for (int j = 0; j < nb && ok; ++j) {
+        const int vs = j % L::VS;
+        const uint32_t v_addr = smem_u32(smem + L::OFF_V + vs * L::V_BYTES);
+        const int st = (j + 1) % L::KS;
+        const uint32_t k_addr = smem_u32(smem + L::OFF_K + st * L::K_BYTES);
 #pragma unroll
-          for (int k = 0; k < HD / 16; ++k) {
-            const uint32_t off = (k >> 2) * 16384 + (k & 3) * 32;
-            umma_bf16(s_tmem, sdesc_sw128(q_addr + off), sdesc_sw128(k_addr + off), idesc_s, k > 0);
+        for (int t = 0; t < 2; ++t) {
+          if (!mbar_wait(&bars->p_full[t], j & 1, p.err) ||
+              (t == 0 && !mbar_wait(&bars->v_full[vs], (j / L::VS) & 1, p.err))) {
+            ok = false;
+            break;
           }
-          umma_commit(&bars->s_full[st]);
-          umma_commit(&bars->k_empty[st]);
-        }
-        if (j >= 1) {
-          const int i = j - 1;
-          const int pb = i & 1;
-          if (!mbar_wait(&bars->p_full[pb], (i >> 1) & 1, p.err)) break;
-          if (!mbar_wait(&bars->v_full[pb], (i >> 1) & 1, p.err)) break;
           tc_fence_after();
-          const uint32_t p_addr = smem_u32(smem + L::OFF_P + pb * L::P_BYTES);
-          const uint32_t v_addr = smem_u32(smem + L::OFF_V + pb * L::V_BYTES);
-#pragma unroll
-          for (int k = 0; k < BKV / 16; ++k) {
-            const uint32_t poff = (k >> 2) * 16384 + (k & 3) * 32;
-            const uint32_t voff = (k >> 2) * L::V_PANEL + (k & 3) * 32;
-            umma_bf16(o_tmem, sdesc_sw128(p_addr + poff), sdesc_sw128(v_addr + voff), idesc_o,
-                      (i > 0 || k > 0) ? 1u : 0u);
+          issue_pv<HD>(tmem_base + L::O_COL + t * HD, tmem_base + t * BKV, v_addr, j == 0);
+          umma_commit(&bars->pv_done[t]);
+          if (t == 1) umma_commit(&bars->v_empty[vs]);
+          if (j + 1 < nb) {
+            if ((t == 0 && !mbar_wait(&bars->k_full[st], ((j + 1) / L::KS) & 1, p.err)) ||
+                !mbar_wait(&bars->pv_done[t], j & 1, p.err)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            issue_s<HD>(tmem_base + t * BKV, q_addr + t * L::Q_BYTES, k_addr);
+            umma_commit(&bars->s_full[t]);
+            if (t == 1) umma_commit(&bars->k_empty[st]);
           }
-          umma_commit(&bars->pv_done[pb]);
-          umma_commit(&bars->v_empty[pb]);
         }
       }
       umma_commit(&bars->drain);
       mbar_wait(&bars->drain, 0, p.err);
     }
-  } else if (warp >= 2 && warp <= 5) {
+  } else {
     // ---------------------------------------------------- softmax warps
-    const int quarter = warp & 3;
+    constexpr int HC = BKV / 2;  // score columns per thread
+    constexpr int OC = HD / 2;   // output columns per thread
+    const int idx = warp - 3;    // 0..15
+    const int t = idx >> 3;      // query tile
+    const int half = (idx >> 2) & 1;
+    const int quarter = warp & 3;  // TMEM lane quarter this warp may access
     const int r = quarter * 32 + lane;  // query row within the tile
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-    const uint32_t o_tmem = tmem_base + L::O_COL + lane_off;
+    const uint32_t s_tmem = tmem_base + t * BKV + lane_off;
+    const uint32_t o_tmem = tmem_base + L::O_COL + t * HD + lane_off + half * OC;
+    uint64_t* xbar = &bars->xchg[t][quarter];
+    uint32_t xuses = 0;
+    float* red = reinterpret_cast<float*>(smem + L::OFF_RED) + t * 2 * BQ;
     float m_used = -CUDART_INF_F;
     float l = 0.f;
     bool ok = true;
     for (int j = 0; j < nb; ++j) {
-      const int sb = j & 1;
-      if (!mbar_wait(&bars->s_full[sb], (j >> 1) & 1, p.err)) {
+      if (!mbar_wait(&bars->s_full[t], j & 1, p.err)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      float s[BKV];
+      float s[HC];
       __syncwarp();
-#pragma unroll
-      for (int c = 0; c < BKV / 32; ++c)
-        tmem_ld32(tmem_base + sb * BKV + lane_off + c * 32,
-                  *reinterpret_cast<float(*)[32]>(&s[c * 32]));
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->s_free[sb]);
+      tmem_ld64(s_tmem + half * HC, s);
 
-      const int kv0 = j * BKV;
-      if (kv0 + BKV > p.s_len) {
+      const int kv0 = ((j + kb0) % nb) * BKV + half * HC;
+      if (kv0 + HC > p.s_len) {
 #pragma unroll
-        for (int c = 0; c < BKV; ++c)
+        for (int c = 0; c < HC; ++c)
           if (kv0 + c >= p.s_len) s[c] = -CUDART_INF_F;
       }
-      float mx = s[0];
+      float m8[8];
 #pragma unroll
-      for (int c = 1; c < BKV; ++c) mx = fmaxf(mx, s[c]);
-      mx *= p.scale_log2;
+      for (int c = 0; c < 8; ++c) m8[c] = s[c];
+#pragma unroll
+      for (int c = 8; c < HC; ++c) m8[c & 7] = fmaxf(m8[c & 7], s[c]);
+      const float lmax = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                               fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+      // The exchange also orders the two halves' reads of S_t before either
+      // overwrites S_t's columns with P_t below.
+      red[half * BQ + r] = lmax;
+      if (!pair_sync(xbar, xuses, p.err)) {
+        ok = false;
+        break;
+      }
+      const float omax = red[(1 - half) * BQ + r];
+      if (!pair_sync(xbar, xuses, p.err)) {  // both have read before the next write
+        ok = false;
+        break;
+      }
+      const float mx = fmaxf(lmax, omax) * p.scale_log2;
 
       const bool need = mx > m_used + RESCALE_LOG2;
       if (__any_sync(0xffffffffu, need) && j > 0) {
-        // O holds PV_0 .. PV_{j-1}; wait for the last one, then rescale rows
-        // whose maximum moved (alpha = 1 for the others).
+        // O_t holds PV up to block j - 1, complete: S_t(j) was issued after it.
         const float alpha = need ? ex2_approx(m_used - mx) : 1.0f;
-        if (!mbar_wait(&bars->pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, p.err)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
         __syncwarp();
 #pragma unroll 1
-        for (int c = 0; c < HD / 32; ++c) {
-          float t[32];
-          tmem_ld32(o_tmem + c * 32, t);
+        for (int c = 0; c < OC / 16; ++c) {
+          float tv[16];
+          tmem_ld16(o_tmem + c * 16, tv);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) t[i] *= alpha;
-          tmem_st32(o_tmem + c * 32, t);
+          for (int i = 0; i < 16; ++i) tv[i] *= alpha;
+          tmem_st16(o_tmem + c * 16, tv);
         }
         l *= alpha;
       }
       if (need) m_used = mx;
 
-      float rs = 0.f;
+      // P_t(j) in bf16, two per 32-bit column, into the first half of S_t's
+      // columns: this half's 64 keys land in columns [32 half, 32 half + 32).
+      float r8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int c = 0; c < BKV; ++c) {
-        s[c] = ex2_approx(fmaf(s[c], p.scale_log2, -m_used));
-        rs += s[c];
-      }
-      l += rs;
-
-      // P buffer sb was last read by PV_{j-2}.
-      if (j >= 2 && !mbar_wait(&bars->pv_done[sb], ((j - 2) >> 1) & 1, p.err)) {
-        ok = false;
-        break;
-      }
-      uint8_t* pbase = smem + L::OFF_P + sb * L::P_BYTES;
+      for (int ch = 0; ch < HC / 32; ++ch) {
+        uint32_t pk[16];
 #pragma unroll
-      for (int pn = 0; pn < 2; ++pn)
-#pragma unroll
-        for (int ch = 0; ch < 8; ++ch) {
-          const int k0 = pn * 64 + ch * 8;
-          uint4 u;
-          u.x = pack_bf16x2(s[k0 + 0], s[k0 + 1]);
-          u.y = pack_bf16x2(s[k0 + 2], s[k0 + 3]);
-          u.z = pack_bf16x2(s[k0 + 4], s[k0 + 5]);
-          u.w = pack_bf16x2(s[k0 + 6], s[k0 + 7]);
-          *reinterpret_cast<uint4*>(pbase + pn * 16384 + r * 128 + ((ch ^ (r & 7)) << 4)) = u;
+        for (int c = 0; c < 32; c += 2) {
+          const float e0 = ex2_approx(fmaf(s[ch * 32 + c], p.scale_log2, -m_used));
+          const float e1 = ex2_approx(fmaf(s[ch * 32 + c + 1], p.scale_log2, -m_used));
+          r8[c & 7] += e0;
+          r8[(c + 1) & 7] += e1;
+          pk[c / 2] = pack_bf16x2(e0, e1);
         }
-      fence_proxy_async_smem();
+        __syncwarp();
+        tmem_st16u(s_tmem + half * (HC / 2) + ch * 16, pk);
+      }
+      l += ((r8[0] + r8[1]) + (r8[2] + r8[3])) + ((r8[4] + r8[5]) + (r8[6] + r8[7]));
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->p_full[sb]);
+      if (lane == 0) mbar_arrive(&bars->p_full[t]);
     }
     if (ok) {
-      const int i = nb - 1;
-      if (mbar_wait(&bars->pv_done[i & 1], (i >> 1) & 1, p.err)) {
+      if (mbar_wait(&bars->pv_done[t], (nb - 1) & 1, p.err)) {
         tc_fence_after();
-        const float inv_l = 1.0f / l;
-        const int row = q0 + r;
-        __nv_bfloat16* dst = p.o + ((size_t)seq * p.s_len + row) * p.ldo + h * HD;
+        red[half * BQ + r] = l;
+        pair_sync(xbar, xuses, p.err);
+        const float inv_l = 1.0f / (l + red[(1 - half) * BQ + r]);
+        const int row = q0 + t * BQ + r;
+        __nv_bfloat16* dst = p.o + ((size_t)seq * p.s_len + row) * p.ldo + h * HD + half * OC;
         __syncwarp();
 #pragma unroll 1
-        for (int c = 0; c < HD / 32; ++c) {
-          float t[32];
-          tmem_ld32(o_tmem + c * 32, t);
+        for (int c = 0; c < OC / 32; ++c) {
+          float tv[32];
+          tmem_ld32(o_tmem + c * 32, tv);
           if (row < p.s_len) {
 #pragma unroll
-            for (int e = 0; e < 32; ++e) t[e] *= inv_l;
+            for (int e = 0; e < 32; ++e) tv[e] *= inv_l;
             uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
               uint4 u;
-              u.x = pack_bf16x2(t[8 * q + 0], t[8 * q + 1]);
-              u.y = pack_bf16x2(t[8 * q + 2], t[8 * q + 3]);
-              u.z = pack_bf16x2(t[8 * q + 4], t[8 * q + 5]);
-              u.w = pack_bf16x2(t[8 * q + 6], t[8 * q + 7]);
+              u.x = pack_bf16x2(tv[8 * q + 0], tv[8 * q + 1]);
+              u.y = pack_bf16x2(tv[8 * q + 2], tv[8 * q + 3]);
+              u.z = pack_bf16x2(tv[8 * q + 4], tv[8 * q + 5]);
+              u.w = pack_bf16x2(tv[8 * q + 6], tv[8 * q + 7]);
               d4[q] = u;
             }
           }
@@ -363,29 +441,35 @@ cudaError_t launch_attention(int hd, const __nv_bfloat16* qk, const __nv_bfloat1
   if (!ds) return cudaErrorInitializationError;
   const int s_len = n_tokens / n_seqs;
   const int s_pad = (s_len + 7) & ~7;
-  const uint64_t cqk = (uint64_t)(nh + nkv) * hd;
   CUtensorMap tq, tv;
   {
-    const uint64_t dims[3] = {cqk, (uint64_t)s_len, (uint64_t)n_seqs};
-    const uint64_t strides[2] = {cqk * 2, cqk * 2 * (uint64_t)s_len};
-    const uint32_t box[3] = {64, BQ, 1};
-    if (!make_tmap_bf16(&tq, qk, 3, dims, strides, box)) return cudaErrorInvalidValue;
+    // q/k head-major [head][seq][token][d] as a 2D view: x = d, y = row of
+    // (head * n_seqs + seq) * s_len + token.  A box that runs past the end
+    // of a sequence reads the next sequence's rows: those keys are masked
+    // and those query rows are never stored.
+    const uint64_t dims[2] = {(uint64_t)hd, (uint64_t)(nh + nkv) * n_tokens};
+    const uint64_t strides[1] = {(uint64_t)hd * 2};
+    const uint32_t box[2] = {64, BQ};
+    if (!make_tmap_bf16(&tq, qk, 2, dims, strides, box)) return cudaErrorInvalidValue;
   }
   {
-    const uint64_t dims[3] = {(uint64_t)s_len, (uint64_t)nkv * hd, (uint64_t)n_seqs};
-    const uint64_t strides[2] = {(uint64_t)s_pad * 2, (uint64_t)s_pad * 2 * nkv * hd};
-    const uint32_t box[3] = {64, (uint32_t)hd, 1};
-    if (!make_tmap_bf16(&tv, vt, 3, dims, strides, box)) return cudaErrorInvalidValue;
+    // v transposed [seq][g][c][s_pad] as a 2D view: x = key (only s_len of
+    // the s_pad columns exist, the rest read as zero), y = (seq nkv + g) d + c
+    const uint64_t dims[2] = {(uint64_t)s_len, (uint64_t)n_seqs * nkv * hd};
+    const uint64_t strides[1] = {(uint64_t)s_pad * 2};
+    const uint32_t box[2] = {64, (uint32_t)hd};
+    if (!make_tmap_bf16(&tv, vt, 2, dims, strides, box)) return cudaErrorInvalidValue;
   }
   AttnParams p;
   p.o = o;
   p.ldo = nh * hd;
   p.s_len = s_len;
+  p.n_seqs = n_seqs;
   p.nh = nh;
   p.nkv = nkv;
   p.scale_log2 = (float)(1.4426950408889634 / sqrt((double)hd));
   p.err = dev_err(ds);
-  dim3 grid((s_len + BQ - 1) / BQ, nh, n_seqs);
+  dim3 grid((s_len + 2 * BQ - 1) / (2 * BQ), nh, n_seqs);
   if (hd == 64) return launch_hd<64>(tq, tv, p, grid, st);
   if (hd == 128) return launch_hd<128>(tq, tv, p, grid, st);
   return cudaErrorInvalidValue;

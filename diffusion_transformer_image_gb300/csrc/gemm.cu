@@ -18,7 +18,8 @@
 //   EPI_RESIDUAL  x += gate * y on the fp32 residual stream (out, down)
 //   EPI_SWIGLU    h = SiLU(gate) * up, gate and up columns in one tile
 //   EPI_QKV       per-head LayerNorm of q and k with gain/bias, then RoPE;
-//                 v written transposed per sequence for the attention kernel
+//                 q and k written head-major, v transposed per sequence, the
+//                 layouts the attention kernel loads as contiguous tiles
 #include "internal.h"
 
 namespace dit {
@@ -192,7 +193,9 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, uint32_t tbas
             }
           }
         }
-        __nv_bfloat16* dst = q.qk + (size_t)row * q.ldqk + col0;
+        // head-major: one head's rows are contiguous, so an attention tile of
+        // 128 tokens x d is one contiguous block
+        __nv_bfloat16* dst = q.qk + ((size_t)head * p.M + row) * HD;
 #pragma unroll
         for (int c = 0; c < HD / 32; ++c)
           store_bf16x32(dst + c * 32, *reinterpret_cast<float(*)[32]>(&v[c * 32]));

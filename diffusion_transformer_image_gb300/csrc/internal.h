@@ -36,8 +36,7 @@ enum GemmEpi : int {
 };
 
 struct QkvEpi {
-  __nv_bfloat16* qk;   // [M, (nh + nkv) hd]
-  int ldqk;
+  __nv_bfloat16* qk;   // [nh + nkv][M][hd], q heads then k heads
   __nv_bfloat16* vt;   // [n_seqs, nkv, hd, s_pad]
   int s_len, s_pad;
   int nh, nkv;

@@ -254,7 +254,9 @@ def dit_qkv_rope(cfg: BlockConfig, w: DeviceBlock, a, rope_cos, rope_sin, qk, vt
 
 
 def dit_attention(cfg: BlockConfig, qk, vt, o, n_seqs=1, stream=None):
-    _check(lib.dit_attention(ctypes.byref(cfg), _ptr(qk), _ptr(vt), qk.shape[0], n_seqs, _ptr(o),
+    """qk: [n_heads + n_kv_heads, n_tokens, d] bf16 (head-major); vt as written
+    by dit_qkv_rope; o: [n_tokens, n_heads * d] bf16."""
+    _check(lib.dit_attention(ctypes.byref(cfg), _ptr(qk), _ptr(vt), o.shape[0], n_seqs, _ptr(o),
                              _stream(stream)), "dit_attention")
     return o
 

@@ -193,7 +193,8 @@ dit_status dit_linear(int32_t epilogue, const void* a, int64_t lda, const void* 
  * section VI, the fused per-head norm then rotation): [q|k|v] = a Wqkv^T, then per head
  * q <- RoPE(LN_d(q) q_g + q_b), k likewise, v unchanged.
  * a: device bf16 [n_tokens, H].  Outputs:
- *   qk: device bf16 [n_tokens, (n_heads + n_kv_heads) d], q heads then k heads
+ *   qk: device bf16 [n_heads + n_kv_heads][n_tokens][d], head-major: q heads
+ *       then k heads, each head's rows contiguous
  *   vt: device bf16 [n_seqs, n_kv_heads, d, s_pad], v transposed per sequence,
  *       s_pad = round_up(n_tokens / n_seqs, 8); columns >= seq length unused. */
 dit_status dit_qkv_rope(const dit_block_config* cfg, const dit_block_weights* w,

@@ -175,13 +175,13 @@ def test_qkv_rope(case):
     blk = dit.DeviceBlock(dict(w, w_o=w["w_qkv"], w_gu=w["w_qkv"], w_down=w["w_qkv"]), dev())
     rc = torch.from_numpy(np.cos(ang)).to(dev())
     rs = torch.from_numpy(np.sin(ang)).to(dev())
-    qk = torch.zeros(n, (nh + nkv) * hd, dtype=torch.bfloat16, device=dev())
+    qk = torch.zeros(nh + nkv, n, hd, dtype=torch.bfloat16, device=dev())
     vt = torch.zeros(ns, nkv, hd, s_pad, dtype=torch.bfloat16, device=dev())
     dit.dit_qkv_rope(cfg, blk, a.to(dev()), rc, rs, qk, vt, n_seqs=ns)
     ow = {k: npf(v) for k, v in w.items()}
     q, k, v = O.qkv_heads(ocfg, npf(a), ow, np.tile(ang, (ns, 1)))
-    gq = npf(qk)[:, : nh * hd].reshape(n, nh, hd)
-    gk = npf(qk)[:, nh * hd:].reshape(n, nkv, hd)
+    gq = npf(qk)[:nh].transpose(1, 0, 2)      # head-major -> [n, nh, hd]
+    gk = npf(qk)[nh:].transpose(1, 0, 2)
     gv = npf(vt)[..., :S].transpose(0, 3, 1, 2).reshape(n, nkv, hd)
     for got, ref in ((gq, q), (gk, k), (gv, v)):
         np.testing.assert_allclose(got, ref, rtol=BF16_REL, atol=2e-3 * _rms(ref))
@@ -209,7 +209,7 @@ def test_attention(case):
         kf = kf * ramp[:, None, None]
     k = kf.to(torch.bfloat16)
     v = bf16_normal((n, nkv, hd), f"at_v{case}")
-    qk = torch.cat([q.reshape(n, nh * hd), k.reshape(n, nkv * hd)], 1).contiguous()
+    qk = torch.cat([q.permute(1, 0, 2), k.permute(1, 0, 2)], 0).contiguous()  # head-major
     vt = torch.zeros(ns, nkv, hd, s_pad, dtype=torch.bfloat16)
     vt[..., :S] = v.reshape(ns, S, nkv, hd).permute(0, 2, 3, 1)
     o = torch.full((n, nh * hd), float("nan"), dtype=torch.bfloat16, device=dev())
