@@ -150,17 +150,17 @@ def traffic_for(kernel_key):
 
 
 # ------------------------------------------------------------- oracle arm
-def cpu_oracle_sample(wl, seed=0):
-    """Times the CPU oracle on one of the 36 layers plus the conditioning,
-    patch embedding and final projection; returns (ms per full step scaled to
-    36 layers, sample description, threads)."""
+def cpu_oracle_sample(wl, seed=0, n_sample_layers=2):
+    """Times the CPU oracle on `n_sample_layers` of the model's layers plus the
+    conditioning, patch embedding, final projection and Euler update at full
+    size; returns (ms per full step with the layer time scaled to all layers,
+    sample description, threads)."""
     import numpy as np
     from diffusion_transformer_image_gb300 import synth
     from oracle import dit_oracle as O
 
-    mw = synth.model_weights(wl, seed=seed, n_layers=1)
+    mw = synth.model_weights(wl, seed=seed, n_layers=n_sample_layers)
     ow = {k: synth.to_numpy_f32(v) for k, v in mw.items() if k != "layers"}
-    lw = {k: synth.to_numpy_f32(v) for k, v in mw["layers"][0].items()}
     latent = synth.latent_input(wl, seed=1).numpy()
     text = synth.text_input(wl, seed=1).float().numpy()
     bc = O.BlockConfig(wl.hidden, wl.n_heads, wl.n_kv_heads, wl.head_dim, wl.ffn)
@@ -171,14 +171,22 @@ def cpu_oracle_sample(wl, seed=0):
     ang = O.rope_angles_3d(O.position_ids(wl.grid_h, wl.grid_w, wl.n_txt), wl.rope_axes,
                            wl.rope_theta)
     t1 = time.perf_counter()
-    x = O.block_forward(bc, lw, x, mod, ang)
+    layer_s = 0.0
+    for li in range(n_sample_layers):
+        lw = {k: synth.to_numpy_f32(v) for k, v in mw["layers"][li].items()}
+        ta = time.perf_counter()
+        x = O.block_forward(bc, lw, x, mod, ang)
+        layer_s += time.perf_counter() - ta
     t2 = time.perf_counter()
     v = O.final_layer(x[: wl.grid_h * wl.grid_w], fin, ow["out_w"], ow["out_b"], bc.ln_eps)
     O.euler_step(latent, v, s[0], s[1])
     t3 = time.perf_counter()
-    ms = ((t1 - t0) + (t3 - t2) + wl.n_layers * (t2 - t1)) * 1e3
-    sample = (f"1 of {wl.n_layers} layers + conditioning, patch embed, final projection and "
-              f"Euler update at full size, layer time x{wl.n_layers}; {t3 - t0:.1f} s of CPU work")
+    per_layer = layer_s / n_sample_layers
+    ms = ((t1 - t0) + (t3 - t2) + wl.n_layers * per_layer) * 1e3
+    work = (t1 - t0) + layer_s + (t3 - t2)
+    sample = (f"{n_sample_layers} of {wl.n_layers} layers + conditioning, patch embed, final "
+              f"projection and Euler update at full size, mean layer time x{wl.n_layers}; "
+              f"{work:.1f} s of CPU work")
     return ms, sample, os.cpu_count()
 
 
@@ -414,6 +422,41 @@ def run_ours(args, rank, world, local):
             "peak_source": f"{peak_src} bf16_tflops_sustained",
             "algorithmic": f"{per_block[dom]:.4e} FLOP per launch"}
 
+    # HBM-bound kernels on buffers far larger than L2 (their per-block sizes
+    # above are partly L2-resident and launch-bound): LayerNorm + modulate
+    # on [65536, 4096] (6 B per element) and the Euler update on 2^28
+    # elements (12 B per element), through the same C-ABI entry points.
+    def time_ms(f, reps=10):
+        f()
+        torch.cuda.synchronize()
+        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a0.record(stream)
+        for _ in range(reps):
+            f()
+        a1.record(stream)
+        torch.cuda.synchronize()
+        return a0.elapsed_time(a1) / reps
+
+    hbm = {}
+    big_rows = 65536
+    xb = torch.randn(big_rows, wl.hidden, device=dev)
+    ab = torch.empty(big_rows, wl.hidden, device=dev, dtype=torch.bfloat16)
+    ms_ln = time_ms(lambda: dit.dit_ln_modulate(0, xb, mod[0], mod[1], 1e-6, ab))
+    gbs = 6.0 * big_rows * wl.hidden / (ms_ln * 1e-3) / 1e9
+    hbm["ln_modulate"] = {"shape": [big_rows, wl.hidden], "ms": round(ms_ln, 4),
+                          "achieved": round(gbs, 1), "unit": "GB/s",
+                          "frac": round(gbs / hbm_peak, 3)}
+    del xb, ab
+    ne = 1 << 28
+    xe = torch.randn(ne, device=dev)
+    ve = torch.randn(ne, device=dev)
+    ms_eu = time_ms(lambda: dit.flowmatch_euler_step(xe, ve, sig[0], sig[1]))
+    gbs = 12.0 * ne / (ms_eu * 1e-3) / 1e9
+    hbm["euler"] = {"elements": ne, "ms": round(ms_eu, 4), "achieved": round(gbs, 1),
+                    "unit": "GB/s", "frac": round(gbs / hbm_peak, 3)}
+    del xe, ve
+    hbm["peak_source"] = f"{peak_src} hbm_gbs"
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         ms_cpu, sample, cores = cpu_oracle_sample(wl)
@@ -436,6 +479,7 @@ def run_ours(args, rank, world, local):
             "gpu_launches": launches,
             "roofline": roof,
             "kernels": kernels,
+            "hbm_kernels_large": hbm,
             "cpu_baseline": cpu,
         }
         print(json.dumps(line), flush=True)

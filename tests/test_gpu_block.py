@@ -198,9 +198,23 @@ def oracle_model_config(wl, n_layers):
                          rope_axes=wl.rope_axes, rope_theta=wl.rope_theta)
 
 
+class _LazyLayers:
+    """Per-layer oracle weights converted on access, so a 36-layer model never
+    sits in host memory as fp32 all at once."""
+
+    def __init__(self, layers):
+        self.layers = layers
+
+    def __len__(self):
+        return len(self.layers)
+
+    def __getitem__(self, i):
+        return oracle_weights(self.layers[i])
+
+
 def oracle_model_weights(mw):
     out = {k: synth.to_numpy_f32(v) for k, v in mw.items() if k != "layers"}
-    out["layers"] = [oracle_weights(l) for l in mw["layers"]]
+    out["layers"] = _LazyLayers(mw["layers"])
     return out
 
 
