@@ -61,8 +61,15 @@ class BlockConfig:
     ffn: int
     rope_layout: str = "interleaved"   # "interleaved" (DiT) or "half" (ViT)
     adaln: bool = True                  # 6-way AdaLN modulation + gates
-    qk_norm: bool = True                # per-head LayerNorm on q and k
+    qk_norm: bool = True                # per-head norm on q and k
     ln_eps: float = 1e-6
+    # Variants of the block as the ERNIE page draws it ([ERNIE] §IV per-layer
+    # graph, §V Bug 1) and of the gates the zml-flow-rs page discovers
+    # ([ZFLOW] §IV, §V).  The defaults are the workload's block.
+    norm_kind: str = "layer"            # "layer" or "rms": pre-norms, qk-norm, final norm
+    glu: str = "silu"                   # "silu" or "gelu_tanh" (clamped tanh GELU)
+    rope_order: str = "norm_rope"       # "norm_rope" or "rope_norm"
+    gate_fn: str = "identity"           # "identity", "tanh" or "sigmoid"
 
 
 @dataclass
@@ -106,6 +113,50 @@ def layer_norm(x: np.ndarray, eps: float) -> np.ndarray:
     d = x - mean
     var = (d * d).mean(axis=-1, keepdims=True, dtype=F32)
     return (d / np.sqrt(var + F32(eps))).astype(F32)
+
+
+def rms_norm(x: np.ndarray, eps: float) -> np.ndarray:
+    """RMSNorm over the last axis without affine: v / sqrt(mean(v^2) + eps)
+    (the norm the ERNIE page draws for AdaLN-Zero and qk-norm, [ERNIE] §IV)."""
+    x = x.astype(F32, copy=False)
+    ms = (x * x).mean(axis=-1, keepdims=True, dtype=F32)
+    return (x / np.sqrt(ms + F32(eps))).astype(F32)
+
+
+def norm(x: np.ndarray, eps: float, kind: str) -> np.ndarray:
+    """The block's norm: LayerNorm or RMSNorm (BlockConfig.norm_kind)."""
+    if kind == "layer":
+        return layer_norm(x, eps)
+    if kind == "rms":
+        return rms_norm(x, eps)
+    raise ValueError(kind)
+
+
+def gelu_tanh_clamped(x: np.ndarray) -> np.ndarray:
+    """GELU by its tanh approximation with the two clamps of [ERNIE] §V Bug 1:
+    a = sqrt(2/pi) (x + 0.044715 x^3) limited to [-20, 20] (tanh is already
+    saturated there, and the limit keeps half-precision tanh finite), then
+    0.5 x (1 + tanh a) limited to the half-precision range [-65504, 65504]."""
+    x = x.astype(F32, copy=False)
+    k = F32(0.7978845608)
+    a = np.clip(k * (x + F32(0.044715) * x * x * x), F32(-20.0), F32(20.0)).astype(F32)
+    y = F32(0.5) * x * (F32(1.0) + np.tanh(a))
+    return np.clip(y, F32(-65504.0), F32(65504.0)).astype(F32)
+
+
+def gate_act(g: np.ndarray, fn: str) -> np.ndarray:
+    """The gate function applied to a modulation gate before it scales its
+    branch: identity (ERNIE, [ERNIE] §VII Decision 1), tanh (Qwen-Image,
+    [ZFLOW] §IV) or sigmoid (Krea-2, [ZFLOW] §V)."""
+    g = g.astype(F32, copy=False)
+    if fn == "identity":
+        return g
+    if fn == "tanh":
+        return np.tanh(g).astype(F32)
+    if fn == "sigmoid":
+        with np.errstate(over="ignore"):
+            return (F32(1.0) / (F32(1.0) + np.exp(-g))).astype(F32)
+    raise ValueError(fn)
 
 
 def modulate(xn: np.ndarray, shift: np.ndarray, scale: np.ndarray) -> np.ndarray:
@@ -254,23 +305,37 @@ def attention_rows(q_rows: np.ndarray, k: np.ndarray, v: np.ndarray, n_heads: in
 # One block
 # --------------------------------------------------------------------------
 def qkv_heads(cfg: BlockConfig, a: np.ndarray, w: dict, angles: np.ndarray):
-    """QKV projection, per-head qk-LayerNorm (gain, bias over head_dim), then
-    RoPE on q and k ([ERNIE] §IV per-layer graph; order norm-then-RoPE per
-    [ZFLOW] §VI, the fused per-head norm then rotation).  Returns q [N,nh,d], k, v [N,nkv,d]."""
+    """QKV projection, per-head qk-norm (gain, bias over head_dim) and RoPE
+    on q and k ([ERNIE] §IV per-layer graph).  Order norm-then-RoPE by
+    default ([ZFLOW] §VI, the fused per-head norm then rotation); the ERNIE
+    page draws RoPE then qk-norm (rope_order "rope_norm").  Returns
+    q [N,nh,d], k, v [N,nkv,d]."""
     nh, nkv, d = cfg.n_heads, cfg.n_kv_heads, cfg.head_dim
     n = a.shape[0]
     qkv = linear(a, w["w_qkv"])
     q = qkv[:, : nh * d].reshape(n, nh, d)
     k = qkv[:, nh * d: (nh + nkv) * d].reshape(n, nkv, d)
     v = qkv[:, (nh + nkv) * d:].reshape(n, nkv, d)
-    if cfg.qk_norm:
-        q = layer_norm(q, cfg.ln_eps) * w["q_g"] + w["q_b"]
-        k = layer_norm(k, cfg.ln_eps) * w["k_g"] + w["k_b"]
-    # angles are per token; broadcast over heads
-    qt = rope_apply(np.swapaxes(q, 0, 1), angles, cfg.rope_layout)
-    kt = rope_apply(np.swapaxes(k, 0, 1), angles, cfg.rope_layout)
-    return (np.ascontiguousarray(np.swapaxes(qt, 0, 1)),
-            np.ascontiguousarray(np.swapaxes(kt, 0, 1)), v.astype(F32))
+    def qk_norm(t, g, b):
+        return norm(t, cfg.ln_eps, cfg.norm_kind) * g + b
+
+    def rotate(t):  # angles are per token; broadcast over heads
+        return np.ascontiguousarray(np.swapaxes(
+            rope_apply(np.swapaxes(t, 0, 1), angles, cfg.rope_layout), 0, 1))
+
+    if cfg.rope_order == "norm_rope":
+        if cfg.qk_norm:
+            q = qk_norm(q, w["q_g"], w["q_b"])
+            k = qk_norm(k, w["k_g"], w["k_b"])
+        q, k = rotate(q), rotate(k)
+    elif cfg.rope_order == "rope_norm":
+        q, k = rotate(q), rotate(k)
+        if cfg.qk_norm:
+            q = qk_norm(q, w["q_g"], w["q_b"])
+            k = qk_norm(k, w["k_g"], w["k_b"])
+    else:
+        raise ValueError(cfg.rope_order)
+    return q.astype(F32), k.astype(F32), v.astype(F32)
 
 
 def block_forward(cfg: BlockConfig, w: dict, x: np.ndarray,
@@ -292,22 +357,31 @@ def block_forward(cfg: BlockConfig, w: dict, x: np.ndarray,
         angles = np.tile(angles, (n // angles.shape[0], 1))
     if cfg.adaln:
         shift1, scale1, gate1, shift2, scale2, gate2 = (mod[i] for i in range(6))
-        a = modulate(layer_norm(x, cfg.ln_eps), shift1, scale1)
+        gate1, gate2 = gate_act(gate1, cfg.gate_fn), gate_act(gate2, cfg.gate_fn)
+        a = modulate(norm(x, cfg.ln_eps, cfg.norm_kind), shift1, scale1)
     else:
         gate1 = gate2 = None
-        a = layer_norm(x, cfg.ln_eps) * w["ln1_g"] + w["ln1_b"]
+        a = norm(x, cfg.ln_eps, cfg.norm_kind) * w["ln1_g"] + w["ln1_b"]
     q, k, v = qkv_heads(cfg, a, w, angles)
     o = attention(q, k, v, cfg.n_heads, cfg.n_kv_heads, n_seqs)
     x = gated_residual(x, gate1, linear(o, w["w_o"]))
     if cfg.adaln:
-        a = modulate(layer_norm(x, cfg.ln_eps), shift2, scale2)
+        a = modulate(norm(x, cfg.ln_eps, cfg.norm_kind), shift2, scale2)
     else:
-        a = layer_norm(x, cfg.ln_eps) * w["ln2_g"] + w["ln2_b"]
-    gu = linear(a, w["w_gu"])
-    f = cfg.ffn
-    h = silu(gu[:, :f]) * gu[:, f:]
-    x = gated_residual(x, gate2, linear(h.astype(F32), w["w_down"]))
+        a = norm(x, cfg.ln_eps, cfg.norm_kind) * w["ln2_g"] + w["ln2_b"]
+    x = gated_residual(x, gate2, linear(glu(cfg, linear(a, w["w_gu"])), w["w_down"]))
     return x
+
+
+def glu(cfg: BlockConfig, gu: np.ndarray) -> np.ndarray:
+    """The gated FFN activation on the stacked gate/up projection (gate
+    columns first): SiLU(gate) * up ([ZFLOW] §VI, SwiGLU) or the clamped
+    tanh GELU(gate) * up ([ERNIE] §IV and §V Bug 1)."""
+    f = cfg.ffn
+    act = silu if cfg.glu == "silu" else gelu_tanh_clamped
+    if cfg.glu not in ("silu", "gelu_tanh"):
+        raise ValueError(cfg.glu)
+    return (act(gu[:, :f]) * gu[:, f:]).astype(F32)
 
 
 def block_forward_rows(cfg: BlockConfig, w: dict, x: np.ndarray, mod: Optional[np.ndarray],
@@ -319,21 +393,19 @@ def block_forward_rows(cfg: BlockConfig, w: dict, x: np.ndarray, mod: Optional[n
     x = x.astype(F32, copy=False)
     if cfg.adaln:
         shift1, scale1, gate1, shift2, scale2, gate2 = (mod[i] for i in range(6))
-        a = modulate(layer_norm(x, cfg.ln_eps), shift1, scale1)
+        gate1, gate2 = gate_act(gate1, cfg.gate_fn), gate_act(gate2, cfg.gate_fn)
+        a = modulate(norm(x, cfg.ln_eps, cfg.norm_kind), shift1, scale1)
     else:
         gate1 = gate2 = None
-        a = layer_norm(x, cfg.ln_eps) * w["ln1_g"] + w["ln1_b"]
+        a = norm(x, cfg.ln_eps, cfg.norm_kind) * w["ln1_g"] + w["ln1_b"]
     q, k, v = qkv_heads(cfg, a, w, angles)
     o = attention_rows(q[rows], k, v, cfg.n_heads, cfg.n_kv_heads)
     xr = gated_residual(x[rows], gate1, linear(o, w["w_o"]))
     if cfg.adaln:
-        a2 = modulate(layer_norm(xr, cfg.ln_eps), shift2, scale2)
+        a2 = modulate(norm(xr, cfg.ln_eps, cfg.norm_kind), shift2, scale2)
     else:
-        a2 = layer_norm(xr, cfg.ln_eps) * w["ln2_g"] + w["ln2_b"]
-    gu = linear(a2, w["w_gu"])
-    f = cfg.ffn
-    h = silu(gu[:, :f]) * gu[:, f:]
-    return gated_residual(xr, gate2, linear(h.astype(F32), w["w_down"]))
+        a2 = norm(xr, cfg.ln_eps, cfg.norm_kind) * w["ln2_g"] + w["ln2_b"]
+    return gated_residual(xr, gate2, linear(glu(cfg, linear(a2, w["w_gu"])), w["w_down"]))
 
 
 # --------------------------------------------------------------------------
@@ -392,12 +464,12 @@ def euler_step(x: np.ndarray, v: np.ndarray, sigma: float, sigma_next: float) ->
 # Whole denoise step (DiT) and ViT forward
 # --------------------------------------------------------------------------
 def final_layer(x_img: np.ndarray, fin: np.ndarray, w_out: np.ndarray,
-                b_out: np.ndarray, eps: float) -> np.ndarray:
+                b_out: np.ndarray, eps: float, kind: str = "layer") -> np.ndarray:
     """AdaLN-continuous final norm and output projection: chunk order
     [scale, shift] ([ERNIE] §V Bug 4), then the linear back to the latent
-    channels."""
+    channels.  The norm kind follows the blocks'."""
     scale, shift = fin[0], fin[1]
-    return linear(modulate(layer_norm(x_img, eps), shift, scale), w_out, b_out)
+    return linear(modulate(norm(x_img, eps, kind), shift, scale), w_out, b_out)
 
 
 def denoise_step(mc: ModelConfig, mw: dict, latent: np.ndarray, text: np.ndarray,
@@ -422,7 +494,7 @@ def denoise_step(mc: ModelConfig, mw: dict, latent: np.ndarray, text: np.ndarray
     nl = mc.n_layers if n_layers is None else n_layers
     for li in range(nl):
         x = block_forward(bc, layers[li], x, mod, angles)
-    v = final_layer(x[:n_img], fin, mw["out_w"], mw["out_b"], bc.ln_eps)
+    v = final_layer(x[:n_img], fin, mw["out_w"], mw["out_b"], bc.ln_eps, bc.norm_kind)
     new = euler_step(latent, v, sigma, sigma_next)
     return (new, v) if return_velocity else new
 

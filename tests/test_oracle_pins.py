@@ -448,3 +448,125 @@ def test_block_forward_rows_matches_block_forward(adaln):
     full = O.block_forward(cfg, w, x, mod if adaln else None, ang)
     np.testing.assert_allclose(O.block_forward_rows(cfg, w, x, mod if adaln else None, ang, rows),
                                full[rows], rtol=1e-5, atol=1e-5)
+
+
+# ------------------------------------------------ variants of the block
+def test_rms_norm_hand_example_and_scale():
+    y = O.rms_norm(np.array([[1, 2, 3, 4]], F32), 0.0)
+    np.testing.assert_allclose(y[0], np.array([1, 2, 3, 4]) / math.sqrt(7.5), rtol=1e-6)
+    x = rnd(8, 64) + 3.0
+    r = O.rms_norm(x, 0.0)
+    np.testing.assert_allclose((r.astype(np.float64) ** 2).mean(axis=1), 1.0, rtol=1e-5)
+    np.testing.assert_allclose(O.rms_norm(-2.5 * x, 0.0), -r, rtol=1e-5, atol=1e-6)
+    # unlike LayerNorm, a constant offset is not removed
+    assert np.abs(O.rms_norm(x, 1e-6).mean(axis=1)).min() > 0.5
+
+
+def test_gelu_tanh_clamped_closed_forms():
+    g = lambda v: float(O.gelu_tanh_clamped(np.array([v], F32))[0])
+    assert g(0.0) == 0.0
+    # GELU(1) by the tanh form: 0.5 (1 + tanh(0.7978845608 * 1.044715))
+    assert abs(g(1.0) - 0.5 * (1 + math.tanh(0.7978845608 * 1.044715))) < 1e-6
+    # odd part: gelu(x) - gelu(-x) = x exactly for the tanh form
+    for v in (0.3, 1.7, 4.0):
+        assert abs(g(v) - g(-v) - v) < 1e-5
+    # close to the exact x Phi(x) (the tanh form's error is below 1e-3)
+    for v in np.linspace(-6, 6, 49):
+        exact = 0.5 * v * (1 + math.erf(v / math.sqrt(2)))
+        assert abs(g(float(v)) - exact) < 1e-3
+    # the argument clamp: tanh saturates, large inputs pass through, large
+    # negative ones vanish; the output clamp at the half-precision maximum
+    assert g(30.0) == 30.0 and abs(g(-30.0)) < 1e-12
+    assert g(1e5) == 65504.0 and abs(g(-1e5)) < 1e-12
+
+
+def test_gate_functions():
+    g = np.array([0.0, math.log(3.0), math.atanh(0.5)], F32)
+    np.testing.assert_array_equal(O.gate_act(g, "identity"), g)
+    t = O.gate_act(g, "tanh")
+    assert t[0] == 0.0 and abs(t[2] - 0.5) < 1e-6
+    s = O.gate_act(g, "sigmoid")
+    assert s[0] == 0.5 and abs(s[1] - 0.75) < 1e-6
+
+
+def test_block_sigmoid_gate_at_zero_is_half_identity_gate():
+    # sigmoid(0) = 1/2: a block with sigmoid gates and zero gate inputs equals
+    # the identity-gate block with gates of exactly 1/2.
+    cfg_s = tiny_cfg(gate_fn="sigmoid")
+    cfg_i = tiny_cfg()
+    w = tiny_weights(cfg_s)
+    x, mod, pos = tiny_inputs()
+    ang = O.rope_angles_3d(pos, AXES, 256.0)
+    m0 = mod.copy()
+    m0[2] = 0.0
+    m0[5] = 0.0
+    mh = mod.copy()
+    mh[2] = 0.5
+    mh[5] = 0.5
+    np.testing.assert_array_equal(O.block_forward(cfg_s, w, x, m0, ang), O.block_forward(cfg_i, w, x, mh, ang))
+    # tanh(0) = 0: zero gates still give the identity
+    np.testing.assert_array_equal(O.block_forward(tiny_cfg(gate_fn="tanh"), w, x, m0, ang), x)
+
+
+def test_rope_norm_order():
+    w_cfg = tiny_cfg()
+    w = tiny_weights(w_cfg)
+    x, mod, pos = tiny_inputs()
+    ang = O.rope_angles_3d(pos, AXES, 256.0)
+    a = O.modulate(O.layer_norm(x, 1e-6), mod[0], mod[1])
+    w1 = dict(w)
+    w1["q_g"] = np.ones_like(w["q_g"])
+    w1["q_b"] = np.zeros_like(w["q_b"])
+    # LayerNorm after RoPE: the returned q is itself zero-mean, unit-variance
+    q, _, _ = O.qkv_heads(tiny_cfg(rope_order="rope_norm"), a, w1, ang)
+    assert np.abs(q.mean(axis=-1)).max() < 1e-5 and np.abs(q.var(axis=-1) - 1).max() < 1e-3
+    # RMSNorm commutes with a rotation (norms are preserved) when g = 1, b = 0
+    q1, k1, _ = O.qkv_heads(tiny_cfg(norm_kind="rms"), a, w1 | {"k_g": w1["q_g"], "k_b": w1["q_b"]}, ang)
+    q2, k2, _ = O.qkv_heads(tiny_cfg(norm_kind="rms", rope_order="rope_norm"), a,
+                            w1 | {"k_g": w1["q_g"], "k_b": w1["q_b"]}, ang)
+    np.testing.assert_allclose(q1, q2, rtol=1e-4, atol=1e-5)
+    np.testing.assert_allclose(k1, k2, rtol=1e-4, atol=1e-5)
+    # with a non-uniform gain the two orders differ
+    q3, _, _ = O.qkv_heads(tiny_cfg(norm_kind="rms", rope_order="rope_norm"), a, w, ang)
+    q4, _, _ = O.qkv_heads(tiny_cfg(norm_kind="rms"), a, w, ang)
+    assert np.abs(q3 - q4).max() > 1e-2
+
+
+def test_block_geglu_gate_first():
+    # as the SwiGLU test: gate rows read feature 0 with weight -100, so the
+    # clamped GELU of the gate is ~0 and the FFN adds nothing
+    cfg = tiny_cfg(glu="gelu_tanh")
+    w = tiny_weights(cfg)
+    w["w_gu"][:] = 0.0
+    w["w_gu"][: cfg.ffn, 0] = -100.0
+    w["w_gu"][cfg.ffn:, 0] = 1.0
+    x, mod, pos = tiny_inputs()
+    mod[2] = 0.0
+    mod[3] = 0.0
+    mod[3, 0] = 1.0
+    mod[4] = -1.0
+    mod[5] = 1.0
+    ang = O.rope_angles_3d(pos, AXES, 256.0)
+    np.testing.assert_allclose(O.block_forward(cfg, w, x, mod, ang), x, atol=1e-6)
+    # and with the halves swapped the FFN is active
+    w["w_gu"][: cfg.ffn, 0] = 1.0
+    w["w_gu"][cfg.ffn:, 0] = -100.0
+    assert np.abs(O.block_forward(cfg, w, x, mod, ang) - x).max() > 1.0
+
+
+def test_ernie_variant_block_invariants():
+    # With RoPE before the qk-norm, relative-position invariance needs unit
+    # gains and zero biases (a per-dimension gain after the rotation would
+    # break it); RMSNorm then divides each rotated vector by its own length.
+    cfg = tiny_cfg(norm_kind="rms", glu="gelu_tanh", rope_order="rope_norm")
+    w = tiny_weights(cfg)
+    for n in ("q", "k"):
+        w[n + "_g"] = np.ones_like(w[n + "_g"])
+        w[n + "_b"] = np.zeros_like(w[n + "_b"])
+    x, mod, pos = tiny_inputs()
+    ang = O.rope_angles_3d(pos, AXES, 256.0)
+    a = O.block_forward(cfg, w, x, mod, ang)
+    b = O.block_forward(cfg, w, x, mod, O.rope_angles_3d(pos + np.array([4, 1, 3], np.int32), AXES, 256.0))
+    np.testing.assert_allclose(a, b, rtol=1e-4, atol=1e-4)
+    rows = np.array([2, 0, 9])
+    np.testing.assert_allclose(O.block_forward_rows(cfg, w, x, mod, ang, rows), a[rows], rtol=1e-5, atol=1e-5)
