@@ -422,10 +422,6 @@ def run_ours(args, rank, world, local):
             "peak_source": f"{peak_src} bf16_tflops_sustained",
             "algorithmic": f"{per_block[dom]:.4e} FLOP per launch"}
 
-    # HBM-bound kernels on buffers far larger than L2 (their per-block sizes
-    # above are partly L2-resident and launch-bound): LayerNorm + modulate
-    # on [65536, 4096] (6 B per element) and the Euler update on 2^28
-    # elements (12 B per element), through the same C-ABI entry points.
     def time_ms(f, reps=10):
         f()
         torch.cuda.synchronize()
@@ -437,6 +433,26 @@ def run_ours(args, rank, world, local):
         torch.cuda.synchronize()
         return a0.elapsed_time(a1) / reps
 
+    # Whole-block time of the workload's block and of the variant the ERNIE
+    # page draws (RMSNorm, RoPE then qk-norm, clamped tanh-GELU GLU), same
+    # weights and shapes, through dit_block_forward.
+    variants = {}
+    bws = dit.workspace(dit.dit_block_workspace_bytes(dit.block_config_from(wl), wl.n_tokens), dev)
+    for vname, kw in (("workload_block", {}),
+                      ("ernie_as_drawn_block", dict(norm_kind="rms", rope_order="rope_norm",
+                                                    glu="gelu_tanh"))):
+        vcfg = dit.block_config(wl.hidden, wl.n_heads, wl.n_kv_heads, wl.head_dim, wl.ffn, **kw)
+        xv = x.clone()
+        ms_v = time_ms(lambda: dit.dit_block_forward(vcfg, model.blocks[0], xv, mod, rc, rs, ws=bws),
+                       reps=5)
+        variants[vname] = {"ms_per_block": round(ms_v, 4),
+                           "tflops": round(sum(per_block.values()) / (ms_v * 1e-3) / 1e12, 1)}
+    del bws
+
+    # HBM-bound kernels on buffers far larger than L2 (their per-block sizes
+    # above are partly L2-resident and launch-bound): LayerNorm + modulate
+    # on [65536, 4096] (6 B per element) and the Euler update on 2^28
+    # elements (12 B per element), through the same C-ABI entry points.
     hbm = {}
     big_rows = 65536
     xb = torch.randn(big_rows, wl.hidden, device=dev)
@@ -480,6 +496,7 @@ def run_ours(args, rank, world, local):
             "roofline": roof,
             "kernels": kernels,
             "hbm_kernels_large": hbm,
+            "block_variants": variants,
             "cpu_baseline": cpu,
         }
         print(json.dumps(line), flush=True)

@@ -96,6 +96,9 @@ dit_status check_block_config(const dit_block_config* c) {
   if (c->ffn % 128 != 0) return DIT_EUNSUPPORTED;
   if (c->rope_layout != 0 && c->rope_layout != 1) return DIT_EINVAL;
   if (!(c->ln_eps >= 0.0f)) return DIT_EINVAL;
+  if (c->norm_kind < 0 || c->norm_kind > 1 || c->glu_act < 0 || c->glu_act > 1 ||
+      c->rope_order < 0 || c->rope_order > 1 || c->gate_fn < 0 || c->gate_fn > 2)
+    return DIT_EINVAL;
   return DIT_OK;
 }
 
@@ -148,8 +151,14 @@ dit_status run_qkv(const dit_block_config* c, const dit_block_weights* w, const 
   p.qkv.rcos = rc;
   p.qkv.rsin = rs;
   p.qkv.rope_half = c->rope_layout;
+  p.qkv.rms = c->norm_kind;
+  p.qkv.rope_first = c->rope_order;
   p.qkv.eps = c->ln_eps;
   return cuda_status(launch_gemm(EPI_QKV, hd, a, c->hidden, w->w_qkv, c->hidden, p, st));
+}
+
+int residual_epi(int gate_fn) {
+  return gate_fn == 1 ? EPI_RESIDUAL_TANH : gate_fn == 2 ? EPI_RESIDUAL_SIGMOID : EPI_RESIDUAL;
 }
 
 dit_status block_forward_impl(const dit_block_config* c, const dit_block_weights* w, float* x,
@@ -157,9 +166,10 @@ dit_status block_forward_impl(const dit_block_config* c, const dit_block_weights
                               const float* rs, const BlockWs& ws, cudaStream_t st) {
   const int H = c->hidden, hd = c->head_dim, F = c->ffn;
   const bool ada = c->adaln != 0;
+  const int ln_mode = (ada ? 0 : 1) | (c->norm_kind ? 2 : 0);
   cudaError_t e;
-  // a = LN(x) (1 + scale1) + shift1   |   LN(x) g1 + b1
-  e = launch_ln_modulate(ada ? 0 : 1, x, H, n_tokens, H, ada ? mod : w->ln1_g,
+  // a = norm(x) (1 + scale1) + shift1   |   norm(x) g1 + b1
+  e = launch_ln_modulate(ln_mode, x, H, n_tokens, H, ada ? mod : w->ln1_g,
                          ada ? mod + H : w->ln1_b, c->ln_eps, ws.a, H, st);
   if (e != cudaSuccess) return DIT_ECUDA;
   dit_status s = run_qkv(c, w, ws.a, n_tokens, n_seqs, rc, rs, ws.qk, ws.vt, st);
@@ -174,10 +184,10 @@ dit_status block_forward_impl(const dit_block_config* c, const dit_block_weights
     p.out = x;
     p.ldo = H;
     p.vec = ada ? mod + 2 * H : nullptr;
-    e = launch_gemm(EPI_RESIDUAL, 0, ws.o, p.K, w->w_o, p.K, p, st);
+    e = launch_gemm(residual_epi(ada ? c->gate_fn : 0), 0, ws.o, p.K, w->w_o, p.K, p, st);
     if (e != cudaSuccess) return DIT_ECUDA;
   }
-  e = launch_ln_modulate(ada ? 0 : 1, x, H, n_tokens, H, ada ? mod + 3 * H : w->ln2_g,
+  e = launch_ln_modulate(ln_mode, x, H, n_tokens, H, ada ? mod + 3 * H : w->ln2_g,
                          ada ? mod + 4 * H : w->ln2_b, c->ln_eps, ws.a, H, st);
   if (e != cudaSuccess) return DIT_ECUDA;
   {  // h = SiLU(a Wg^T) (a Wu^T)
@@ -187,7 +197,7 @@ dit_status block_forward_impl(const dit_block_config* c, const dit_block_weights
     p.K = H;
     p.out = ws.h;
     p.ldo = F;
-    e = launch_gemm(EPI_SWIGLU, 0, ws.a, H, w->w_gu, H, p, st);
+    e = launch_gemm(c->glu_act ? EPI_GEGLU : EPI_SWIGLU, 0, ws.a, H, w->w_gu, H, p, st);
     if (e != cudaSuccess) return DIT_ECUDA;
   }
   {  // x += gate2 (h Wd^T)
@@ -198,7 +208,7 @@ dit_status block_forward_impl(const dit_block_config* c, const dit_block_weights
     p.out = x;
     p.ldo = H;
     p.vec = ada ? mod + 5 * H : nullptr;
-    e = launch_gemm(EPI_RESIDUAL, 0, ws.h, F, w->w_down, F, p, st);
+    e = launch_gemm(residual_epi(ada ? c->gate_fn : 0), 0, ws.h, F, w->w_down, F, p, st);
     if (e != cudaSuccess) return DIT_ECUDA;
   }
   return DIT_OK;
@@ -426,8 +436,8 @@ dit_status dit_denoise_step(const dit_model_config* cfg, const dit_model_weights
   }
   // v = (LN(x_img) (1 + scale_f) + shift_f) Wout^T + bout; fin = [scale, shift].
   // The fp32 norm output enters the tensor core as hi + lo bf16 halves.
-  if (launch_ln_modulate(0, ws.x, H, n_img, H, ws.fin + H, ws.fin, c->ln_eps, bws.a, H, st,
-                         ws.fin_lo) != cudaSuccess)
+  if (launch_ln_modulate(c->norm_kind ? 2 : 0, ws.x, H, n_img, H, ws.fin + H, ws.fin, c->ln_eps,
+                         bws.a, H, st, ws.fin_lo) != cudaSuccess)
     return DIT_ECUDA;
   float* v = velocity_out ? velocity_out : ws.v;
   {
@@ -467,14 +477,17 @@ dit_status flowmatch_sigmas(int32_t n_steps, float shift, float* out_host) {
 dit_status dit_linear(int32_t epilogue, const void* a, int64_t lda, const void* w, int64_t ldw,
                       int32_t M, int32_t N, int32_t K, void* out, int64_t ldo,
                       const float* bias_or_gate, void* stream) {
-  if (epilogue < DIT_EPI_BF16 || epilogue > DIT_EPI_SWIGLU) return DIT_EINVAL;
+  if (epilogue < DIT_EPI_BF16 || epilogue > DIT_EPI_RESIDUAL_SIGMOID) return DIT_EINVAL;
   if (!a || !w || !out || M <= 0 || N <= 0 || K <= 0) return DIT_EINVAL;
   if (K % 8 || lda < K || ldw < K || lda % 8 || ldw % 8) return DIT_EINVAL;
   if (!aligned16(a) || !aligned16(w) || !aligned16(out)) return DIT_EINVAL;
   if (bias_or_gate && !aligned16(bias_or_gate)) return DIT_EINVAL;
-  const bool f32_out = epilogue == DIT_EPI_F32_BIAS || epilogue == DIT_EPI_RESIDUAL;
+  const bool glu = epilogue == DIT_EPI_SWIGLU || epilogue == DIT_EPI_GEGLU;
+  const bool resid = epilogue == DIT_EPI_RESIDUAL || epilogue == DIT_EPI_RESIDUAL_TANH ||
+                     epilogue == DIT_EPI_RESIDUAL_SIGMOID;
+  const bool f32_out = epilogue == DIT_EPI_F32_BIAS || resid;
   if (ldo < N || ldo % (f32_out ? 4 : 8)) return DIT_EINVAL;
-  if (epilogue == DIT_EPI_SWIGLU && N % 128) return DIT_EUNSUPPORTED;
+  if (glu && N % 128) return DIT_EUNSUPPORTED;
   if (!device_state()) return DIT_ECUDA;
   GemmParams p{};
   p.M = M;
@@ -482,8 +495,12 @@ dit_status dit_linear(int32_t epilogue, const void* a, int64_t lda, const void* 
   p.K = K;
   p.out = out;
   p.ldo = ldo;
-  p.vec = epilogue == DIT_EPI_SWIGLU ? nullptr : bias_or_gate;
-  return cuda_status(launch_gemm(epilogue, 0, a, lda, w, ldw, p, static_cast<cudaStream_t>(stream)));
+  p.vec = glu ? nullptr : bias_or_gate;
+  const int kind = epilogue == DIT_EPI_GEGLU            ? EPI_GEGLU
+                   : epilogue == DIT_EPI_RESIDUAL_TANH    ? EPI_RESIDUAL_TANH
+                   : epilogue == DIT_EPI_RESIDUAL_SIGMOID ? EPI_RESIDUAL_SIGMOID
+                                                          : epilogue;
+  return cuda_status(launch_gemm(kind, 0, a, lda, w, ldw, p, static_cast<cudaStream_t>(stream)));
 }
 
 dit_status dit_qkv_rope(const dit_block_config* cfg, const dit_block_weights* w, const void* a,
@@ -521,7 +538,7 @@ dit_status dit_attention(const dit_block_config* cfg, const void* qk, const void
 
 dit_status dit_ln_modulate(int32_t mode, const float* x, int64_t ldx, int32_t rows, int32_t H,
                            const float* p0, const float* p1, float eps, void* out, void* stream) {
-  if ((mode != 0 && mode != 1) || !x || !p0 || !p1 || !out || rows < 0 || H <= 0) return DIT_EINVAL;
+  if (mode < 0 || mode > 3 || !x || !p0 || !p1 || !out || rows < 0 || H <= 0) return DIT_EINVAL;
   if (H % 4 || ldx < H || ldx % 4) return DIT_EINVAL;
   if (H > 8192) return DIT_EUNSUPPORTED;
   if (!aligned16(x) || !aligned16(p0) || !aligned16(p1) || !aligned16(out)) return DIT_EINVAL;

@@ -17,6 +17,8 @@
 //   EPI_F32_BIAS  fp32 store with bias (patch embedding, output projection)
 //   EPI_RESIDUAL  x += gate * y on the fp32 residual stream (out, down)
 //   EPI_SWIGLU    h = SiLU(gate) * up, gate and up columns in one tile
+//   EPI_GEGLU     the same with the clamped tanh GELU ([ERNIE] section V, Bug 1)
+//   EPI_RESIDUAL_TANH / _SIGMOID  x += f(gate) * y ([ZFLOW] sections IV, V)
 //   EPI_QKV       per-head LayerNorm of q and k with gain/bias, then RoPE;
 //                 q and k written head-major, v transposed per sequence, the
 //                 layouts the attention kernel loads as contiguous tiles
@@ -58,12 +60,62 @@ __device__ __forceinline__ void store_bf16x32(__nv_bfloat16* dst, const float (&
 
 __device__ __forceinline__ float silu_f(float x) { return x / (1.0f + expf(-x)); }
 
+// GELU by its tanh approximation, the argument limited to [-20, 20] and the
+// result to [-65504, 65504] ([ERNIE] section V, Bug 1).
+__device__ __forceinline__ float gelu_tanh_clamped_f(float x) {
+  float a = 0.7978845608f * (x + 0.044715f * x * x * x);
+  a = fminf(fmaxf(a, -20.0f), 20.0f);
+  const float y = 0.5f * x * (1.0f + tanhf(a));
+  return fminf(fmaxf(y, -65504.0f), 65504.0f);
+}
+
+// The gate function of a gated residual: identity, tanh or sigmoid.
+template <int EPI>
+__device__ __forceinline__ float gate_f(float g) {
+  if constexpr (EPI == EPI_RESIDUAL_TANH) return tanhf(g);
+  if constexpr (EPI == EPI_RESIDUAL_SIGMOID) return 1.0f / (1.0f + expf(-g));
+  return g;
+}
+
+template <int EPI>
+constexpr bool is_residual() {
+  return EPI == EPI_RESIDUAL || EPI == EPI_RESIDUAL_TANH || EPI == EPI_RESIDUAL_SIGMOID;
+}
+
+// Rotates the pairs of one head row by the RoPE table row of its token:
+// pairs (2k, 2k+1) or (k, k + HD/2), angle k.
+template <int HD>
+__device__ __forceinline__ void rope_row(float (&v)[HD], const QkvEpi& q, int row) {
+  const int trow = row % q.s_len;
+  const float4* cs = reinterpret_cast<const float4*>(q.rcos + (size_t)trow * (HD / 2));
+  const float4* sn = reinterpret_cast<const float4*>(q.rsin + (size_t)trow * (HD / 2));
+#pragma unroll
+  for (int k4 = 0; k4 < HD / 8; ++k4) {
+    const float4 c4 = __ldg(cs + k4), s4 = __ldg(sn + k4);
+    const float cc[4] = {c4.x, c4.y, c4.z, c4.w};
+    const float ssn[4] = {s4.x, s4.y, s4.z, s4.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int k = 4 * k4 + e;
+      if (q.rope_half) {
+        const float a = v[k], bb = v[k + HD / 2];
+        v[k] = a * cc[e] - bb * ssn[e];
+        v[k + HD / 2] = a * ssn[e] + bb * cc[e];
+      } else {
+        const float a = v[2 * k], bb = v[2 * k + 1];
+        v[2 * k] = a * cc[e] - bb * ssn[e];
+        v[2 * k + 1] = a * ssn[e] + bb * cc[e];
+      }
+    }
+  }
+}
+
 // ---------------------------------------------------------------- epilogues
 template <int EPI, int HD>
 __device__ __forceinline__ void epilogue_tile(const GemmParams& p, uint32_t tbase, int row,
                                               int n_blk) {
   const bool row_ok = row < p.M;
-  if constexpr (EPI == EPI_BF16 || EPI == EPI_F32_BIAS || EPI == EPI_RESIDUAL) {
+  if constexpr (EPI == EPI_BF16 || EPI == EPI_F32_BIAS || is_residual<EPI>()) {
 #pragma unroll 1
     for (int c = 0; c < BN / 32; ++c) {
       const int col = n_blk * BN + c * 32;
@@ -100,14 +152,20 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, uint32_t tbas
           for (int i = 0; i < 32 && col + i < p.N; ++i)
             dst[i] = v[i] + (p.vec ? __ldg(p.vec + col + i) : 0.0f);
         }
-      } else {  // EPI_RESIDUAL
+      } else {  // gated residual
         float* dst = reinterpret_cast<float*>(p.out) + (size_t)row * p.ldo + col;
         if (full) {
 #pragma unroll
           for (int q = 0; q < 8; ++q) {
             float4 x = reinterpret_cast<float4*>(dst)[q];
             float4 g = make_float4(1.f, 1.f, 1.f, 1.f);
-            if (p.vec) g = __ldg(reinterpret_cast<const float4*>(p.vec + col) + q);
+            if (p.vec) {
+              g = __ldg(reinterpret_cast<const float4*>(p.vec + col) + q);
+              g.x = gate_f<EPI>(g.x);
+              g.y = gate_f<EPI>(g.y);
+              g.z = gate_f<EPI>(g.z);
+              g.w = gate_f<EPI>(g.w);
+            }
             x.x = fmaf(g.x, v[4 * q + 0], x.x);
             x.y = fmaf(g.y, v[4 * q + 1], x.y);
             x.z = fmaf(g.z, v[4 * q + 2], x.z);
@@ -116,11 +174,11 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, uint32_t tbas
           }
         } else {
           for (int i = 0; i < 32 && col + i < p.N; ++i)
-            dst[i] = fmaf(p.vec ? __ldg(p.vec + col + i) : 1.0f, v[i], dst[i]);
+            dst[i] = fmaf(p.vec ? gate_f<EPI>(__ldg(p.vec + col + i)) : 1.0f, v[i], dst[i]);
         }
       }
     }
-  } else if constexpr (EPI == EPI_SWIGLU) {
+  } else if constexpr (EPI == EPI_SWIGLU || EPI == EPI_GEGLU) {
     // Accumulator columns [0, 128) are gate rows, [128, 256) the matching up rows.
 #pragma unroll 1
     for (int c = 0; c < 4; ++c) {
@@ -129,8 +187,13 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, uint32_t tbas
       tmem_ld32(tbase + c * 32, g);
       tmem_ld32(tbase + 128 + c * 32, u);
       if (!row_ok) continue;
+      if constexpr (EPI == EPI_GEGLU) {
 #pragma unroll
-      for (int i = 0; i < 32; ++i) g[i] = silu_f(g[i]) * u[i];
+        for (int i = 0; i < 32; ++i) g[i] = gelu_tanh_clamped_f(g[i]) * u[i];
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) g[i] = silu_f(g[i]) * u[i];
+      }
       __nv_bfloat16* dst =
           reinterpret_cast<__nv_bfloat16*>(p.out) + (size_t)row * p.ldo + n_blk * 128 + c * 32;
       store_bf16x32(dst, g);
@@ -153,11 +216,16 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, uint32_t tbas
         const bool is_q = head < q.nh;
         const float* g = is_q ? q.qg : q.kg;
         const float* b = is_q ? q.qb : q.kb;
+        if (q.rope_first) rope_row<HD>(v, q, row);
         if (g != nullptr) {
-          float s = 0.f;
+          // per-head LayerNorm or RMSNorm over the head_dim values of this row
+          float mean = 0.f;
+          if (!q.rms) {
+            float s = 0.f;
 #pragma unroll
-          for (int i = 0; i < HD; ++i) s += v[i];
-          const float mean = s * (1.0f / HD);
+            for (int i = 0; i < HD; ++i) s += v[i];
+            mean = s * (1.0f / HD);
+          }
           float ss = 0.f;
 #pragma unroll
           for (int i = 0; i < HD; ++i) {
@@ -168,31 +236,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, uint32_t tbas
 #pragma unroll
           for (int i = 0; i < HD; ++i) v[i] = fmaf(v[i] * rstd, __ldg(g + i), __ldg(b + i));
         }
-        const int trow = row % q.s_len;
-        const float4* cs = reinterpret_cast<const float4*>(q.rcos + (size_t)trow * (HD / 2));
-        const float4* sn = reinterpret_cast<const float4*>(q.rsin + (size_t)trow * (HD / 2));
-#pragma unroll
-        for (int k4 = 0; k4 < HD / 8; ++k4) {
-          const float4 c4 = __ldg(cs + k4), s4 = __ldg(sn + k4);
-          const float cc[4] = {c4.x, c4.y, c4.z, c4.w};
-          const float ssn[4] = {s4.x, s4.y, s4.z, s4.w};
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int k = 4 * k4 + e;
-            float a, bb;
-            if (q.rope_half) {
-              a = v[k];
-              bb = v[k + HD / 2];
-              v[k] = a * cc[e] - bb * ssn[e];
-              v[k + HD / 2] = a * ssn[e] + bb * cc[e];
-            } else {
-              a = v[2 * k];
-              bb = v[2 * k + 1];
-              v[2 * k] = a * cc[e] - bb * ssn[e];
-              v[2 * k + 1] = a * ssn[e] + bb * cc[e];
-            }
-          }
-        }
+        if (!q.rope_first) rope_row<HD>(v, q, row);
         // head-major: one head's rows are contiguous, so an attention tile of
         // 128 tokens x d is one contiguous block
         __nv_bfloat16* dst = q.qk + ((size_t)head * p.M + row) * HD;
@@ -265,7 +309,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           uint8_t* sb = sa + A_BYTES;
           mbar_arrive_expect_tx(&bars->full[stage], STAGE_BYTES);
           tma_load_2d(sa, &tmA, &bars->full[stage], kb * BK, m_blk * BM);
-          if constexpr (EPI == EPI_SWIGLU) {
+          if constexpr (EPI == EPI_SWIGLU || EPI == EPI_GEGLU) {
             tma_load_2d(sb, &tmB, &bars->full[stage], kb * BK, n_blk * 128);
             tma_load_2d(sb + B_BYTES / 2, &tmB, &bars->full[stage], kb * BK, p.N + n_blk * 128);
           } else {
@@ -380,14 +424,15 @@ cudaError_t launch_gemm(int epi, int hd, const void* A, long long lda, const voi
     if (!make_tmap_bf16(&ta, A, 2, dims, strides, box)) return cudaErrorInvalidValue;
   }
   {
-    const uint64_t rows = epi == EPI_SWIGLU ? 2ull * p.N : (uint64_t)p.N;
+    const bool glu = epi == EPI_SWIGLU || epi == EPI_GEGLU;
+    const uint64_t rows = glu ? 2ull * p.N : (uint64_t)p.N;
     const uint64_t dims[2] = {(uint64_t)p.K, rows};
     const uint64_t strides[1] = {(uint64_t)ldb * 2};
-    const uint32_t box[2] = {BK, epi == EPI_SWIGLU ? 128u : (uint32_t)BN};
+    const uint32_t box[2] = {BK, glu ? 128u : (uint32_t)BN};
     if (!make_tmap_bf16(&tb, B, 2, dims, strides, box)) return cudaErrorInvalidValue;
   }
   p.num_m = (p.M + BM - 1) / BM;
-  p.num_n = epi == EPI_SWIGLU ? p.N / 128 : (p.N + BN - 1) / BN;
+  p.num_n = (epi == EPI_SWIGLU || epi == EPI_GEGLU) ? p.N / 128 : (p.N + BN - 1) / BN;
   p.err = dev_err(ds);
   const int tiles = p.num_m * p.num_n;
   const int grid = tiles < ds->sm_count ? tiles : ds->sm_count;
@@ -396,6 +441,9 @@ cudaError_t launch_gemm(int epi, int hd, const void* A, long long lda, const voi
     case EPI_F32_BIAS: return launch_impl<EPI_F32_BIAS, 0>(ta, tb, p, grid, st);
     case EPI_RESIDUAL: return launch_impl<EPI_RESIDUAL, 0>(ta, tb, p, grid, st);
     case EPI_SWIGLU: return launch_impl<EPI_SWIGLU, 0>(ta, tb, p, grid, st);
+    case EPI_GEGLU: return launch_impl<EPI_GEGLU, 0>(ta, tb, p, grid, st);
+    case EPI_RESIDUAL_TANH: return launch_impl<EPI_RESIDUAL_TANH, 0>(ta, tb, p, grid, st);
+    case EPI_RESIDUAL_SIGMOID: return launch_impl<EPI_RESIDUAL_SIGMOID, 0>(ta, tb, p, grid, st);
     case EPI_QKV:
       if (hd == 64) return launch_impl<EPI_QKV, 64>(ta, tb, p, grid, st);
       if (hd == 128) return launch_impl<EPI_QKV, 128>(ta, tb, p, grid, st);

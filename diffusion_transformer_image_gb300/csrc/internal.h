@@ -32,7 +32,10 @@ enum GemmEpi : int {
   EPI_F32_BIAS = 1,   // out fp32 = acc + bias
   EPI_RESIDUAL = 2,   // out fp32 += gate * acc
   EPI_SWIGLU = 3,     // out bf16 = silu(acc_gate) * acc_up
-  EPI_QKV = 4         // qk-LayerNorm + RoPE -> qk buffer; v -> transposed buffer
+  EPI_QKV = 4,        // qk-norm + RoPE -> qk buffer; v -> transposed buffer
+  EPI_GEGLU = 5,      // out bf16 = gelu_tanh_clamped(acc_gate) * acc_up
+  EPI_RESIDUAL_TANH = 6,     // out fp32 += tanh(gate) * acc
+  EPI_RESIDUAL_SIGMOID = 7   // out fp32 += sigmoid(gate) * acc
 };
 
 struct QkvEpi {
@@ -43,6 +46,8 @@ struct QkvEpi {
   const float *qg, *qb, *kg, *kb;   // null when there is no qk norm
   const float *rcos, *rsin;         // [s_len, hd/2]
   int rope_half;                    // 0: pairs (2k, 2k+1); 1: pairs (k, k + hd/2)
+  int rms;                          // qk-norm is RMSNorm instead of LayerNorm
+  int rope_first;                   // RoPE before the qk-norm
   float eps;
 };
 
@@ -67,6 +72,7 @@ cudaError_t launch_attention(int hd, const __nv_bfloat16* qk, const __nv_bfloat1
                              cudaStream_t st);
 
 // ------------------------------------------------------------- row ops
+// mode: bit 0 affine (else AdaLN), bit 1 RMSNorm (else LayerNorm)
 cudaError_t launch_ln_modulate(int mode, const float* x, long long ldx, int rows, int H,
                                const float* p0, const float* p1, float eps,
                                __nv_bfloat16* out, long long ldo, cudaStream_t st,

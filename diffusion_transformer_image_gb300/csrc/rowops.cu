@@ -11,14 +11,15 @@ namespace dit {
 namespace {
 
 // ----------------------------------------------------- LayerNorm + modulate
-// LN over the row (biased variance), then AdaLN `n (1 + scale) + shift`
+// LN over the row (biased variance) or RMSNorm, then AdaLN `n (1 + scale) + shift`
 // ([ERNIE] "Porting ERNIE-Image-Turbo to Zig and Metal", section IV and
 // section V, Bug 4; [ZFLOW] section VI `plus_one`: the 1 is added on the
 // device) or the affine `n g + b` of the pre-norm ViT ([MAKEPAD]).  One
 // 128-thread block per row, the row held in registers (H <= 128 * 4 * MAXV),
 // mean and variance by warp shuffles plus one shared-memory exchange.
 constexpr int LN_THREADS = 128;
-constexpr int LN_MAXV = 16;  // float4 per thread: H <= 8192
+constexpr int LN_MAXV = 16;  // float4 per thread: H <= 8192 (8 for H <= 4096: fewer
+                             // registers, more rows in flight per SM)
 
 __device__ __forceinline__ float block_sum_128(float v, float* red) {
 #pragma unroll
@@ -33,7 +34,7 @@ __device__ __forceinline__ float block_sum_128(float v, float* red) {
 // With `out_lo` the result is also kept to about 16 significant bits as the
 // pair hi = bf16(r), lo = bf16(r - hi): two bf16 GEMMs over hi and lo then
 // reproduce an fp32-input linear (used by the fp32 head and tail projections).
-template <int MODE>
+template <int MODE, bool RMS, int MAXV>
 __global__ void __launch_bounds__(LN_THREADS) ln_modulate_kernel(
     const float* __restrict__ x, long long ldx, int rows, int H, const float* __restrict__ p0,
     const float* __restrict__ p1, float eps, __nv_bfloat16* __restrict__ out, long long ldo,
@@ -43,20 +44,21 @@ __global__ void __launch_bounds__(LN_THREADS) ln_modulate_kernel(
   if (row >= rows) return;
   const float4* xr = reinterpret_cast<const float4*>(x + (size_t)row * ldx);
   const int n4 = H >> 2;
-  float4 v[LN_MAXV];
+  float4 v[MAXV];
   float s = 0.f;
 #pragma unroll
-  for (int i = 0; i < LN_MAXV; ++i) {
+  for (int i = 0; i < MAXV; ++i) {
     const int idx = threadIdx.x + LN_THREADS * i;
     if (idx < n4) {
       v[i] = __ldg(xr + idx);
       s += (v[i].x + v[i].y) + (v[i].z + v[i].w);
     }
   }
-  const float mean = block_sum_128(s, red) / (float)H;
+  // RMSNorm keeps the mean (it divides by the root mean square instead)
+  const float mean = RMS ? 0.0f : block_sum_128(s, red) / (float)H;
   float ss = 0.f;
 #pragma unroll
-  for (int i = 0; i < LN_MAXV; ++i) {
+  for (int i = 0; i < MAXV; ++i) {
     const int idx = threadIdx.x + LN_THREADS * i;
     if (idx < n4) {
       v[i].x -= mean; v[i].y -= mean; v[i].z -= mean; v[i].w -= mean;
@@ -68,7 +70,7 @@ __global__ void __launch_bounds__(LN_THREADS) ln_modulate_kernel(
   const float4* a4 = reinterpret_cast<const float4*>(p0);
   const float4* b4 = reinterpret_cast<const float4*>(p1);
 #pragma unroll
-  for (int i = 0; i < LN_MAXV; ++i) {
+  for (int i = 0; i < MAXV; ++i) {
     const int idx = threadIdx.x + LN_THREADS * i;
     if (idx < n4) {
       const float4 a = __ldg(a4 + idx), b = __ldg(b4 + idx);
@@ -316,12 +318,21 @@ cudaError_t launch_ln_modulate(int mode, const float* x, long long ldx, int rows
   if (H > LN_THREADS * 4 * LN_MAXV || (H & 3)) return cudaErrorInvalidValue;
   const int grid = rows;
   if (grid == 0) return cudaSuccess;
-  if (mode == 0)
-    ln_modulate_kernel<0><<<grid, LN_THREADS, 0, st>>>(x, ldx, rows, H, p0, p1, eps, out, ldo,
-                                                       out_lo);
-  else
-    ln_modulate_kernel<1><<<grid, LN_THREADS, 0, st>>>(x, ldx, rows, H, p0, p1, eps, out, ldo,
-                                                       out_lo);
+  const bool small = H <= LN_THREADS * 4 * 8;
+#define DIT_LN_LAUNCH(M, R)                                                                     \
+  (small ? (ln_modulate_kernel<M, R, 8><<<grid, LN_THREADS, 0, st>>>(x, ldx, rows, H, p0, p1, eps, \
+                                                                     out, ldo, out_lo), 0)          \
+         : (ln_modulate_kernel<M, R, LN_MAXV><<<grid, LN_THREADS, 0, st>>>(x, ldx, rows, H, p0, p1, \
+                                                                           eps, out, ldo, out_lo), \
+            0))
+  switch (mode) {
+    case 0: DIT_LN_LAUNCH(0, false); break;
+    case 1: DIT_LN_LAUNCH(1, false); break;
+    case 2: DIT_LN_LAUNCH(0, true); break;
+    case 3: DIT_LN_LAUNCH(1, true); break;
+    default: return cudaErrorInvalidValue;
+  }
+#undef DIT_LN_LAUNCH
   count_launch();
   return cudaGetLastError();
 }

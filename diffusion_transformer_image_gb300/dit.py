@@ -29,6 +29,11 @@ c_float_p = ctypes.POINTER(ctypes.c_float)
 
 DIT_OK, DIT_EINVAL, DIT_EUNSUPPORTED, DIT_EWORKSPACE, DIT_ECUDA, DIT_ETIMEOUT = 0, -1, -2, -3, -4, -5
 DIT_EPI_BF16, DIT_EPI_F32_BIAS, DIT_EPI_RESIDUAL, DIT_EPI_SWIGLU = 0, 1, 2, 3
+DIT_EPI_GEGLU, DIT_EPI_RESIDUAL_TANH, DIT_EPI_RESIDUAL_SIGMOID = 4, 5, 6
+NORM_KINDS = {"layer": 0, "rms": 1}
+GLU_ACTS = {"silu": 0, "gelu_tanh": 1}
+ROPE_ORDERS = {"norm_rope": 0, "rope_norm": 1}
+GATE_FNS = {"identity": 0, "tanh": 1, "sigmoid": 2}
 
 EXPORTED = [
     "dit_block_workspace_bytes", "dit_block_forward", "dit_denoise_workspace_bytes",
@@ -50,7 +55,9 @@ class DitError(RuntimeError):
 class BlockConfig(ctypes.Structure):
     _fields_ = [("hidden", c_int32), ("n_heads", c_int32), ("n_kv_heads", c_int32),
                 ("head_dim", c_int32), ("ffn", c_int32), ("rope_layout", c_int32),
-                ("adaln", c_int32), ("qk_norm", c_int32), ("ln_eps", c_float)]
+                ("adaln", c_int32), ("qk_norm", c_int32), ("ln_eps", c_float),
+                ("norm_kind", c_int32), ("glu_act", c_int32), ("rope_order", c_int32),
+                ("gate_fn", c_int32)]
 
 
 class BlockWeights(ctypes.Structure):
@@ -134,16 +141,19 @@ def _stream(stream=None):
 
 # --------------------------------------------------------------- structures
 def block_config(hidden, n_heads, n_kv_heads, head_dim, ffn, rope_layout="interleaved",
-                 adaln=True, qk_norm=True, ln_eps=1e-6) -> BlockConfig:
+                 adaln=True, qk_norm=True, ln_eps=1e-6, norm_kind="layer", glu="silu",
+                 rope_order="norm_rope", gate_fn="identity") -> BlockConfig:
     return BlockConfig(hidden, n_heads, n_kv_heads, head_dim, ffn,
                        0 if rope_layout == "interleaved" else 1, int(bool(adaln)),
-                       int(bool(qk_norm)), ln_eps)
+                       int(bool(qk_norm)), ln_eps, NORM_KINDS[norm_kind], GLU_ACTS[glu],
+                       ROPE_ORDERS[rope_order], GATE_FNS[gate_fn])
 
 
 def block_config_from(wl) -> BlockConfig:
     """BlockConfig of a synthetic workload description (synth.Workload)."""
     return block_config(wl.hidden, wl.n_heads, wl.n_kv_heads, wl.head_dim, wl.ffn,
-                        wl.rope_layout, wl.adaln, wl.qk_norm)
+                        wl.rope_layout, wl.adaln, wl.qk_norm, norm_kind=wl.norm_kind,
+                        glu=wl.glu, rope_order=wl.rope_order, gate_fn=wl.gate_fn)
 
 
 def model_config_from(wl, n_layers: Optional[int] = None) -> ModelConfig:
@@ -240,7 +250,8 @@ def flowmatch_sigmas(n_steps: int, shift: float) -> list:
 def dit_linear(epilogue: int, a: torch.Tensor, w: torch.Tensor, out: torch.Tensor,
                bias_or_gate=None, n_out: Optional[int] = None, stream=None):
     M, K = a.shape
-    N = n_out if n_out is not None else (w.shape[0] // 2 if epilogue == DIT_EPI_SWIGLU else w.shape[0])
+    glu = epilogue in (DIT_EPI_SWIGLU, DIT_EPI_GEGLU)
+    N = n_out if n_out is not None else (w.shape[0] // 2 if glu else w.shape[0])
     _check(lib.dit_linear(epilogue, _ptr(a), a.stride(0), _ptr(w), w.stride(0), M, N, K, _ptr(out),
                           out.stride(0), _ptr(bias_or_gate), _stream(stream)), "dit_linear")
     return out

@@ -44,6 +44,10 @@ class Workload:
     n_seqs: int = 1          # images per batch (ViT); the DiT uses one sequence
     n_prefix: int = 0        # ViT cls/register tokens per image
     t_block: float = 0.5     # timestep of the single-block workloads
+    norm_kind: str = "layer"  # block variants (see the oracle's BlockConfig)
+    glu: str = "silu"
+    rope_order: str = "norm_rope"
+    gate_fn: str = "identity"
 
     @property
     def seq_len(self) -> int:

@@ -62,8 +62,15 @@ typedef struct {
   int32_t rope_layout;  /* 0: pairs (2k, 2k+1) (DiT); 1: pairs (k, k+d/2) (ViT) */
   int32_t adaln;        /* 1: AdaLN modulation + gated residuals from mod[6,H];
                            0: pre-norm LayerNorm with gain/bias, plain residuals */
-  int32_t qk_norm;      /* 1: per-head LayerNorm with gain/bias on q and k */
-  float ln_eps;         /* LayerNorm epsilon (1e-6) */
+  int32_t qk_norm;      /* 1: per-head norm with gain/bias on q and k */
+  float ln_eps;         /* norm epsilon (1e-6) */
+  /* Variants ([ERNIE] section IV per-layer graph and section V, Bug 1;
+   * [ZFLOW] sections IV and V); zero selects the default in brackets. */
+  int32_t norm_kind;    /* [0] LayerNorm; 1 RMSNorm: pre-norms, qk-norm, final norm */
+  int32_t glu_act;      /* [0] SiLU(gate) up; 1 GELU(gate) up, tanh form with the
+                           argument clamped to +-20 and the output to +-65504 */
+  int32_t rope_order;   /* [0] qk-norm then RoPE; 1 RoPE then qk-norm */
+  int32_t gate_fn;      /* [0] x + g y; 1 x + tanh(g) y; 2 x + sigmoid(g) y */
 } dit_block_config;
 
 /* One block's weights, all device pointers.  Linears bf16 [out, in]:
@@ -183,8 +190,15 @@ dit_status flowmatch_sigmas(int32_t n_steps, float shift, float* out_host);
  *                     NULL = 1) -- the gated residual ([ERNIE] section VII,
  *                     Decision 1)
  *   DIT_EPI_SWIGLU:   w holds [Wg; Wu] ([2F, K], gate rows first), N = F,
- *                     out bf16 [M, F] = SiLU(x Wg^T) * (x Wu^T) */
-enum { DIT_EPI_BF16 = 0, DIT_EPI_F32_BIAS = 1, DIT_EPI_RESIDUAL = 2, DIT_EPI_SWIGLU = 3 };
+ *                     out bf16 [M, F] = SiLU(x Wg^T) * (x Wu^T)
+ *   DIT_EPI_GEGLU, DIT_EPI_RESIDUAL_TANH, DIT_EPI_RESIDUAL_SIGMOID: the
+ *                     variants of the two above (see the enum) */
+enum {
+  DIT_EPI_BF16 = 0, DIT_EPI_F32_BIAS = 1, DIT_EPI_RESIDUAL = 2, DIT_EPI_SWIGLU = 3,
+  DIT_EPI_GEGLU = 4,             /* as SWIGLU with the clamped tanh GELU */
+  DIT_EPI_RESIDUAL_TANH = 5,     /* out += tanh(gate) * y */
+  DIT_EPI_RESIDUAL_SIGMOID = 6   /* out += sigmoid(gate) * y */
+};
 dit_status dit_linear(int32_t epilogue, const void* a, int64_t lda, const void* w,
                       int64_t ldw, int32_t M, int32_t N, int32_t K, void* out,
                       int64_t ldo, const float* bias_or_gate, void* stream);
@@ -210,9 +224,11 @@ dit_status dit_qkv_rope(const dit_block_config* cfg, const dit_block_weights* w,
 dit_status dit_attention(const dit_block_config* cfg, const void* qk, const void* vt,
                          int32_t n_tokens, int32_t n_seqs, void* o, void* stream);
 
-/* LayerNorm over each row of x (biased variance, eps) then
+/* Norm over each row of x then
  *   mode 0 (AdaLN): out = n (1 + p1) + p0   (p0 = shift, p1 = scale)
  *   mode 1 (affine): out = n p0 + p1         (p0 = gain, p1 = bias)
+ * with n = LayerNorm(x) (biased variance, eps); add 2 to the mode for
+ * n = RMSNorm(x) = x / sqrt(mean(x^2) + eps) ([ERNIE] section IV).
  * x: device fp32 [rows, H] (row stride ldx); out: device bf16 [rows, H]. */
 dit_status dit_ln_modulate(int32_t mode, const float* x, int64_t ldx, int32_t rows,
                            int32_t H, const float* p0, const float* p1, float eps,

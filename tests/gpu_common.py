@@ -44,7 +44,9 @@ def cosine(a, b):
 
 def oracle_block_config(wl):
     return O.BlockConfig(wl.hidden, wl.n_heads, wl.n_kv_heads, wl.head_dim, wl.ffn,
-                         rope_layout=wl.rope_layout, adaln=wl.adaln, qk_norm=wl.qk_norm)
+                         rope_layout=wl.rope_layout, adaln=wl.adaln, qk_norm=wl.qk_norm,
+                         norm_kind=wl.norm_kind, glu=wl.glu, rope_order=wl.rope_order,
+                         gate_fn=wl.gate_fn)
 
 
 def oracle_weights(w: dict) -> dict:

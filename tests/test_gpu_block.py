@@ -103,6 +103,61 @@ def test_block_forward_small_strong_modulation(name):
     assert_block_parity(got, ref, what=name)
 
 
+VARIANTS = {
+    # the block as the ERNIE page draws it: RMSNorm, RoPE then qk-norm,
+    # clamped tanh-GELU GLU
+    "ernie_as_drawn": dict(norm_kind="rms", rope_order="rope_norm", glu="gelu_tanh"),
+    "tanh_gate": dict(gate_fn="tanh"),
+    "sigmoid_gate": dict(gate_fn="sigmoid"),
+}
+
+
+def with_variant(wl, **kw):
+    import dataclasses
+    return dataclasses.replace(wl, **kw)
+
+
+@pytest.mark.parametrize("variant", list(VARIANTS))
+@pytest.mark.parametrize("name", ["tiny_block", "gqa_small"])
+def test_block_variants_small(name, variant):
+    wl = with_variant(SMALL_BLOCKS[name], **VARIANTS[variant])
+    w = synth.block_weights(wl, 0, seed=0)
+    x = synth.residual_input(wl, seed=1)
+    mod_g, mod_o = conditioning_pair(wl, wl.t_block)
+    got = run_block_gpu(wl, w, x, mod_g)
+    ref = O.block_forward(oracle_block_config(wl), oracle_weights(w), npf(x), mod_o,
+                          oracle_angles(wl), wl.n_seqs)
+    assert_block_parity(got, ref, what=f"{name}/{variant}")
+
+
+def test_ernie_as_drawn_block_full_size_sampled_rows():
+    """The ERNIE-shaped block as the page draws it, at full size, 74 valid text
+    tokens (4096 + 74 = 4170 rows: ragged GEMM and attention tails) as when the
+    text is truncated to its valid length ([ERNIE] section VII, Decision 2)."""
+    wl = with_variant(synth.WORKLOADS["ernie_block"], n_txt=74, **VARIANTS["ernie_as_drawn"])
+    w = synth.block_weights(wl, 0, seed=0)
+    x = synth.residual_input(wl, seed=1)
+    mod_g, mod_o = conditioning_pair(wl, wl.t_block)
+    got = run_block_gpu(wl, w, x, mod_g)
+    rows = sample_rows(wl.n_tokens)
+    ref = O.block_forward_rows(oracle_block_config(wl), oracle_weights(w), npf(x), mod_o,
+                               oracle_angles(wl), rows)
+    assert_block_parity(got[rows], ref, what="ernie_as_drawn 4170")
+
+
+def test_block_truncated_text_4170_rows():
+    """The workload's block with the text truncated to 74 tokens: 4170 rows."""
+    wl = with_variant(synth.WORKLOADS["ernie_block"], n_txt=74)
+    w = synth.block_weights(wl, 0, seed=0)
+    x = synth.residual_input(wl, seed=1)
+    mod_g, mod_o = conditioning_pair(wl, wl.t_block)
+    got = run_block_gpu(wl, w, x, mod_g)
+    rows = sample_rows(wl.n_tokens)
+    ref = O.block_forward_rows(oracle_block_config(wl), oracle_weights(w), npf(x), mod_o,
+                               oracle_angles(wl), rows)
+    assert_block_parity(got[rows], ref, what="4170 rows")
+
+
 def test_block_zero_gates_pass_through_exactly():
     wl = synth.WORKLOADS["tiny_block"]
     w = synth.block_weights(wl, 0, seed=0)

@@ -246,3 +246,61 @@ def test_invalid_arguments_enqueue_nothing():
     with pytest.raises(dit.DitError) as e:
         dit.dit_block_forward(cfg, None, x, None, x, x, ws=torch.zeros(256, dtype=torch.uint8, device=dev()))
     assert e.value.status in (dit.DIT_EUNSUPPORTED, dit.DIT_EINVAL)
+
+
+# ------------------------------------------------------------- variants
+@pytest.mark.parametrize("rows,H,affine", [(37, 256, False), (130, 4096, False), (69, 1024, True)])
+def test_rms_modulate(rows, H, affine):
+    x = (bf16_normal((rows, H), f"rms_x{rows}_{H}", std=2.0).float() + 0.5)
+    p0 = bf16_normal((H,), f"rms_p0{H}", std=0.5).float()
+    p1 = bf16_normal((H,), f"rms_p1{H}", std=0.5).float()
+    out = torch.empty(rows, H, dtype=torch.bfloat16, device=dev())
+    dit.dit_ln_modulate(3 if affine else 2, x.to(dev()), p0.to(dev()), p1.to(dev()), 1e-6, out)
+    n = O.rms_norm(npf(x), 1e-6)
+    ref = n * npf(p0) + npf(p1) if affine else O.modulate(n, npf(p0), npf(p1))
+    np.testing.assert_allclose(npf(out), ref, rtol=BF16_REL, atol=1e-4)
+
+
+@pytest.mark.parametrize("M,F,K", [(256, 128, 256), (300, 384, 512)])
+def test_linear_geglu(M, F, K):
+    a = bf16_normal((M, K), f"gg_a{M}_{K}")
+    w = bf16_normal((2 * F, K), f"gg_w{F}_{K}", std=0.3)   # large gates reach the clamps
+    out = torch.empty(M, F, dtype=torch.bfloat16, device=dev())
+    dit.dit_linear(dit.DIT_EPI_GEGLU, a.to(dev()), w.to(dev()), out)
+    gu = O.linear(npf(a), npf(w))
+    ref = O.gelu_tanh_clamped(gu[:, :F]) * gu[:, F:]
+    np.testing.assert_allclose(npf(out), ref, rtol=BF16_REL, atol=1e-3 * _rms(ref))
+
+
+@pytest.mark.parametrize("fn", ["tanh", "sigmoid"])
+def test_linear_gated_residual_gate_functions(fn):
+    M, N, K = 300, 256, 512
+    a = bf16_normal((M, K), f"gf_a{fn}")
+    w = bf16_normal((N, K), f"gf_w{fn}", std=0.05)
+    x = bf16_normal((M, N), f"gf_x{fn}").float()
+    g = bf16_normal((N,), f"gf_g{fn}", std=2.0).float()
+    xg = x.to(dev()).contiguous()
+    epi = dit.DIT_EPI_RESIDUAL_TANH if fn == "tanh" else dit.DIT_EPI_RESIDUAL_SIGMOID
+    dit.dit_linear(epi, a.to(dev()), w.to(dev()), xg, g.to(dev()))
+    ref = O.gated_residual(npf(x), O.gate_act(npf(g), fn), O.linear(npf(a), npf(w)))
+    np.testing.assert_allclose(npf(xg), ref, rtol=1e-5, atol=1e-4 * _rms(ref))
+
+
+@pytest.mark.parametrize("kind,order", [("rms", "norm_rope"), ("layer", "rope_norm"), ("rms", "rope_norm")])
+@pytest.mark.parametrize("case", ["mha64", "gqa128_tail"])
+def test_qkv_norm_variants(case, kind, order):
+    cfg, w, a, ang, ocfg, (H, nh, nkv, hd, S, ns) = _qkv_setup(case)
+    cfg.norm_kind = dit.NORM_KINDS[kind]
+    cfg.rope_order = dit.ROPE_ORDERS[order]
+    ocfg.norm_kind, ocfg.rope_order = kind, order
+    n = S * ns
+    s_pad = (S + 7) // 8 * 8
+    blk = dit.DeviceBlock(dict(w, w_o=w["w_qkv"], w_gu=w["w_qkv"], w_down=w["w_qkv"]), dev())
+    rc = torch.from_numpy(np.cos(ang)).to(dev())
+    rs = torch.from_numpy(np.sin(ang)).to(dev())
+    qk = torch.zeros(nh + nkv, n, hd, dtype=torch.bfloat16, device=dev())
+    vt = torch.zeros(ns, nkv, hd, s_pad, dtype=torch.bfloat16, device=dev())
+    dit.dit_qkv_rope(cfg, blk, a.to(dev()), rc, rs, qk, vt, n_seqs=ns)
+    q, k, _ = O.qkv_heads(ocfg, npf(a), {kk: npf(vv) for kk, vv in w.items()}, np.tile(ang, (ns, 1)))
+    for got, ref in ((npf(qk)[:nh].transpose(1, 0, 2), q), (npf(qk)[nh:].transpose(1, 0, 2), k)):
+        np.testing.assert_allclose(got, ref, rtol=BF16_REL, atol=2e-3 * _rms(ref))
