@@ -18,7 +18,8 @@
 //   warps 3..18  softmax, eight per tile: query row r of tile t is shared by
 //                two warps (the same TMEM lane quarter), each owning 64 of
 //                the 128 scores of a block.  They exchange row maxima through
-//                shared memory, keep the running maximum and their partial
+//                shared memory (one barrier meeting per block), keep the
+//                running maximum and their partial
 //                sums, overwrite S_t with P_t (bf16, two per 32-bit column),
 //                and rescale their half of O_t when the maximum grows by more
 //                than 2^8 (smaller growth is absorbed: exponentials stay
@@ -64,8 +65,11 @@ struct AttnLayout {
   static constexpr int OFF_K = OFF_Q + 2 * Q_BYTES;
   static constexpr int OFF_V = OFF_K + KS * K_BYTES;
   static constexpr int OFF_BAR = OFF_V + VS * V_BYTES;
-  static constexpr int OFF_RED = OFF_BAR + 512;   // [tile][half][128 rows] fp32 exchange
-  static constexpr int END = OFF_RED + 2 * 2 * BQ * 4;
+  // Row-maximum exchange between the two softmax warps of a row:
+  // maxima [tile][block parity][half][row] fp32, final sums [tile][half][row].
+  static constexpr int OFF_RED = OFF_BAR + 512;
+  static constexpr int OFF_LSUM = OFF_RED + 2 * 2 * 2 * BQ * 4;
+  static constexpr int END = OFF_LSUM + 2 * 2 * BQ * 4;
   static constexpr int O_COL = 2 * BKV;           // O_A, then O_B
   static_assert(O_COL + 2 * HD <= 512, "TMEM overflow");
 };
@@ -92,9 +96,11 @@ constexpr size_t attn_smem_bytes() {
 // arrives once (lane 0, after the warp's shared-memory writes), then waits for
 // the other.  Bounded like every other wait.
 __device__ __forceinline__ bool pair_sync(uint64_t* bar, uint32_t& uses, const DevErr& e) {
+  tc_fence_before();
   __syncwarp();
   if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
   const bool ok = mbar_wait(bar, uses & 1u, e);
+  tc_fence_after();
   ++uses;
   return ok;
 }
@@ -294,7 +300,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const uint32_t o_tmem = tmem_base + L::O_COL + t * HD + lane_off + half * OC;
     uint64_t* xbar = &bars->xchg[t][quarter];
     uint32_t xuses = 0;
-    float* red = reinterpret_cast<float*>(smem + L::OFF_RED) + t * 2 * BQ;
+    float* red = reinterpret_cast<float*>(smem + L::OFF_RED) + t * 2 * 2 * BQ;
+    float* lsum = reinterpret_cast<float*>(smem + L::OFF_LSUM) + t * 2 * BQ;
     float m_used = -CUDART_INF_F;
     float l = 0.f;
     bool ok = true;
@@ -322,17 +329,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const float lmax = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
                                fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
       // The exchange also orders the two halves' reads of S_t before either
-      // overwrites S_t's columns with P_t below.
-      red[half * BQ + r] = lmax;
+      // overwrites S_t's columns with P_t below.  Maxima alternate between
+      // two slots, so one meeting per block suffices: a slot is rewritten
+      // two blocks later, and the partner read it before its next arrival.
+      float* slot = red + (j & 1) * 2 * BQ;
+      slot[half * BQ + r] = lmax;
       if (!pair_sync(xbar, xuses, p.err)) {
         ok = false;
         break;
       }
-      const float omax = red[(1 - half) * BQ + r];
-      if (!pair_sync(xbar, xuses, p.err)) {  // both have read before the next write
-        ok = false;
-        break;
-      }
+      const float omax = slot[(1 - half) * BQ + r];
       const float mx = fmaxf(lmax, omax) * p.scale_log2;
 
       const bool need = mx > m_used + RESCALE_LOG2;
@@ -377,9 +383,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (ok) {
       if (mbar_wait(&bars->pv_done[t], (nb - 1) & 1, p.err)) {
         tc_fence_after();
-        red[half * BQ + r] = l;
+        lsum[half * BQ + r] = l;
         pair_sync(xbar, xuses, p.err);
-        const float inv_l = 1.0f / (l + red[(1 - half) * BQ + r]);
+        const float inv_l = 1.0f / (l + lsum[(1 - half) * BQ + r]);
         const int row = q0 + t * BQ + r;
         __nv_bfloat16* dst = p.o + ((size_t)seq * p.s_len + row) * p.ldo + h * HD + half * OC;
         __syncwarp();
