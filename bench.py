@@ -73,6 +73,24 @@ def workload_flops(wl, n_layers):
     return per_block, n_layers * sum(per_block.values()) + head_tail
 
 
+def max_over_ranks(value, world, device):
+    """The maximum of a per-rank float over all ranks (identity for one rank)."""
+    if world == 1:
+        return float(value)
+    import torch
+    import torch.distributed as tdist
+    t = torch.tensor([float(value)], device=device, dtype=torch.float64)
+    tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_metrics(elapsed_max_ms, steps, world):
+    """(value, ms per step of one rank): every rank runs `steps` independent
+    denoise steps, so the whole job completes steps * world of them in the
+    slowest rank's time."""
+    return elapsed_max_ms / (steps * world), elapsed_max_ms / steps
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -354,14 +372,38 @@ def run_ours(args, rank, world, local):
     status = dit.dit_last_device_error()
     if status != dit.DIT_OK:
         raise RuntimeError(f"device error word set during the bench: {status}")
-    if world > 1:
-        t = torch.tensor([elapsed_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
-    ms_per_step_rank = elapsed_ms / args.steps
-    value = elapsed_ms / (args.steps * world)
+    elapsed_ms = max_over_ranks(elapsed_ms, world, dev)
+    value, ms_per_step_rank = replica_metrics(elapsed_ms, args.steps, world)
     per_block, step_flops = workload_flops(wl, wl.n_layers)
     tflops = step_flops / (ms_per_step_rank * 1e-3) / 1e12
+
+    # ---- the 8-step loop captured once as a CUDA graph and replayed (the
+    # library allocates nothing and never synchronises, so it captures)
+    graph_ms = None
+    try:
+        lat_g = latent0.clone()
+        g = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream()
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            with torch.cuda.graph(g, stream=side):
+                for i in range(8):
+                    dit.dit_denoise_step(cfg, model, lat_g, text, wl.grid_h, wl.grid_w, sig[i],
+                                         sig[i + 1], ws=ws)
+        stream.wait_stream(side)
+        g.replay()
+        torch.cuda.synchronize()
+        g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        g0.record(stream)
+        reps = max(1, args.steps // 8)
+        for _ in range(reps):
+            g.replay()
+        g1.record(stream)
+        torch.cuda.synchronize()
+        graph_ms = g0.elapsed_time(g1) / (8 * reps)
+        del g
+    except RuntimeError as exc:  # capture unsupported by this torch build: report why
+        graph_ms = f"unavailable: {exc}"
 
     # ---- end to end through the public API with host buffers
     lat_host = latent0.cpu().pin_memory()
@@ -493,6 +535,8 @@ def run_ours(args, rank, world, local):
             "e2e": {"value": round(e2e_ms, 4), "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h},
             "gpu_launches": launches,
+            "graph_replay_ms_per_step": graph_ms if not isinstance(graph_ms, float)
+            else round(graph_ms, 4),
             "roofline": roof,
             "kernels": kernels,
             "hbm_kernels_large": hbm,
