@@ -30,7 +30,12 @@ the design doc with its reason):
   * the FFN is SwiGLU: silu(gate) * up, gate rows first in the stacked weight;
   * gates are applied as plain products (identity gate function);
   * one modulation vector [6, H] is shared by all layers of a step;
-  * image rows come first in the joint sequence, then text rows.
+  * image rows come first in the joint sequence, then text rows;
+  * the W8A8 format with H256 rotation ([ZFLOW] §VII) rotates the
+    contraction axis of both operands in independent 256-wide blocks by the
+    orthonormal Sylvester Hadamard matrix and codes each row with one scale
+    (amax / 448); the 8-bit code is e4m3, the 8-bit type the target tensor
+    cores multiply (they have no integer kind).
 
 Parity pins: every function here is checked by tests/test_oracle_pins.py
 against closed forms, brute force or invariants.  The numeric value of a
@@ -70,6 +75,10 @@ class BlockConfig:
     glu: str = "silu"                   # "silu" or "gelu_tanh" (clamped tanh GELU)
     rope_order: str = "norm_rope"       # "norm_rope" or "rope_norm"
     gate_fn: str = "identity"           # "identity", "tanh" or "sigmoid"
+    # Format of the four projections ([ZFLOW] §VII): "bf16", or "w8a8_h256":
+    # both operands rotated by a 256-point Hadamard along K and coded in 8 bits
+    # with one scale per row.
+    linear_format: str = "bf16"
 
 
 @dataclass
@@ -93,6 +102,110 @@ def linear(x: np.ndarray, w: np.ndarray, b: Optional[np.ndarray] = None) -> np.n
     if b is not None:
         y = y + b.astype(F32, copy=False)
     return y.astype(F32, copy=False)
+
+
+# --------------------------------------------------------------------------
+# Low-precision linears: Hadamard rotation and 8-bit codes ([ZFLOW] §VII)
+# --------------------------------------------------------------------------
+HADAMARD_N = 256
+E4M3_MAX = 448.0
+
+
+def fwht256_rows(x: np.ndarray) -> np.ndarray:
+    """x H along the last axis, in independent blocks of 256, where H is the
+    256-point Sylvester Hadamard matrix scaled by 1/16 (so H H^T = I): the
+    rotation "H256" of [ZFLOW] §VII.  Computed by the fast Walsh-Hadamard
+    transform in float32: eight butterfly stages, span 1, 2, ..., 128, each
+    replacing the pair (u at index i, w at index i + span), i without the span
+    bit, by (u + w, u - w); then one exact multiplication by 1/16."""
+    y = np.array(x, dtype=F32, copy=True)
+    n, k = y.shape
+    if k % HADAMARD_N:
+        raise ValueError("the rotated axis must be a multiple of 256")
+    nb = k // HADAMARD_N
+    span = 1
+    while span < HADAMARD_N:
+        t = y.reshape(n, nb, HADAMARD_N // (2 * span), 2, span)
+        u = t[:, :, :, 0, :].copy()
+        w = t[:, :, :, 1, :].copy()
+        t[:, :, :, 0, :] = u + w
+        t[:, :, :, 1, :] = u - w
+        span *= 2
+    return (y * F32(1.0 / 16.0)).astype(F32)
+
+
+def e4m3_round(v: np.ndarray) -> np.ndarray:
+    """Rounds float32 values to the nearest value of the 8-bit float format
+    e4m3 (1 sign, 4 exponent bits with bias 7, 3 mantissa bits, no infinity,
+    largest finite 448, subnormals in steps of 2^-9), ties to the even
+    mantissa, magnitudes above 448 saturated to 448.  Returns float32 values
+    on that grid (each is one code)."""
+    a = np.abs(v.astype(np.float64))
+    _, e = np.frexp(a)                       # a = m 2^e, m in [0.5, 1)
+    e = np.maximum(e - 1, -6)                # binade exponent; subnormals share -6
+    step = np.ldexp(1.0, e - 3)              # 3 mantissa bits
+    q = np.rint(a / step) * step             # rint: half to even; a / step is exact
+    q = np.minimum(q, E4M3_MAX)
+    return (np.sign(v) * q).astype(F32)
+
+
+def e4m3_decode_table() -> np.ndarray:
+    """The value of each of the 256 e4m3 codes as float32 (code = sign << 7 |
+    exponent << 3 | mantissa); the two NaN codes 0x7f and 0xff map to NaN."""
+    vals = np.empty(256, dtype=F32)
+    for c in range(256):
+        s = -1.0 if c & 0x80 else 1.0
+        e, m = (c >> 3) & 0xF, c & 0x7
+        if e == 15 and m == 7:
+            vals[c] = np.nan
+        elif e == 0:
+            vals[c] = s * m * 2.0 ** -9
+        else:
+            vals[c] = s * (1.0 + m / 8.0) * 2.0 ** (e - 7)
+    return vals
+
+
+def quantize_rows_e4m3(y: np.ndarray):
+    """Per-row 8-bit coding ([ZFLOW] §VII: "per-row" on both operands).
+    For each row: amax = max |y|; scale = amax / 448 and inv = 448 / amax, both
+    one float32 division; code = e4m3_round(y * inv) with the product in
+    float32.  An all-zero row gets scale 0 and zero codes.  Returns (the codes'
+    values as float32 [rows, k], scale float32 [rows]); y ~= code * scale."""
+    y = y.astype(F32, copy=False)
+    amax = np.max(np.abs(y), axis=1).astype(F32)
+    nz = amax > 0
+    safe = np.where(nz, amax, F32(1.0)).astype(F32)
+    scale = np.where(nz, (safe / F32(E4M3_MAX)).astype(F32), F32(0.0)).astype(F32)
+    inv = np.where(nz, (F32(E4M3_MAX) / safe).astype(F32), F32(0.0)).astype(F32)
+    codes = e4m3_round((y * inv[:, None]).astype(F32))
+    return codes, scale
+
+
+def rotate_quantize(x: np.ndarray):
+    """Rotation then per-row coding of one operand: quantize_rows_e4m3 of
+    fwht256_rows(x)."""
+    return quantize_rows_e4m3(fwht256_rows(x))
+
+
+def linear_w8a8_h256(x: np.ndarray, w: np.ndarray) -> np.ndarray:
+    """y = x W^T in the format W8A8 with H256 rotation ([ZFLOW] §VII): by the
+    rotation rule (x H)(W H)^T = x W^T for orthogonal H, both operands are
+    rotated along K and coded per row; y[i, o] = sx[i] sw[o] sum_k qx[i, k]
+    qw[o, k].  The sum of code products is taken in float64, where it is
+    exact for these operand sizes."""
+    qx, sx = rotate_quantize(x)
+    qw, sw = rotate_quantize(w)
+    acc = np.matmul(qx.astype(np.float64), qw.astype(np.float64).T)
+    return (acc * sx.astype(np.float64)[:, None] * sw.astype(np.float64)[None, :]).astype(F32)
+
+
+def project(cfg: "BlockConfig", x: np.ndarray, w: np.ndarray) -> np.ndarray:
+    """One of the block's four projections in the block's linear format."""
+    if cfg.linear_format == "bf16":
+        return linear(x, w)
+    if cfg.linear_format == "w8a8_h256":
+        return linear_w8a8_h256(x, w)
+    raise ValueError(cfg.linear_format)
 
 
 def silu(x: np.ndarray) -> np.ndarray:
@@ -312,7 +425,7 @@ def qkv_heads(cfg: BlockConfig, a: np.ndarray, w: dict, angles: np.ndarray):
     q [N,nh,d], k, v [N,nkv,d]."""
     nh, nkv, d = cfg.n_heads, cfg.n_kv_heads, cfg.head_dim
     n = a.shape[0]
-    qkv = linear(a, w["w_qkv"])
+    qkv = project(cfg, a, w["w_qkv"])
     q = qkv[:, : nh * d].reshape(n, nh, d)
     k = qkv[:, nh * d: (nh + nkv) * d].reshape(n, nkv, d)
     v = qkv[:, (nh + nkv) * d:].reshape(n, nkv, d)
@@ -364,12 +477,12 @@ def block_forward(cfg: BlockConfig, w: dict, x: np.ndarray,
         a = norm(x, cfg.ln_eps, cfg.norm_kind) * w["ln1_g"] + w["ln1_b"]
     q, k, v = qkv_heads(cfg, a, w, angles)
     o = attention(q, k, v, cfg.n_heads, cfg.n_kv_heads, n_seqs)
-    x = gated_residual(x, gate1, linear(o, w["w_o"]))
+    x = gated_residual(x, gate1, project(cfg, o, w["w_o"]))
     if cfg.adaln:
         a = modulate(norm(x, cfg.ln_eps, cfg.norm_kind), shift2, scale2)
     else:
         a = norm(x, cfg.ln_eps, cfg.norm_kind) * w["ln2_g"] + w["ln2_b"]
-    x = gated_residual(x, gate2, linear(glu(cfg, linear(a, w["w_gu"])), w["w_down"]))
+    x = gated_residual(x, gate2, project(cfg, glu(cfg, project(cfg, a, w["w_gu"])), w["w_down"]))
     return x
 
 
@@ -400,12 +513,13 @@ def block_forward_rows(cfg: BlockConfig, w: dict, x: np.ndarray, mod: Optional[n
         a = norm(x, cfg.ln_eps, cfg.norm_kind) * w["ln1_g"] + w["ln1_b"]
     q, k, v = qkv_heads(cfg, a, w, angles)
     o = attention_rows(q[rows], k, v, cfg.n_heads, cfg.n_kv_heads)
-    xr = gated_residual(x[rows], gate1, linear(o, w["w_o"]))
+    xr = gated_residual(x[rows], gate1, project(cfg, o, w["w_o"]))
     if cfg.adaln:
         a2 = modulate(norm(xr, cfg.ln_eps, cfg.norm_kind), shift2, scale2)
     else:
         a2 = norm(xr, cfg.ln_eps, cfg.norm_kind) * w["ln2_g"] + w["ln2_b"]
-    return gated_residual(xr, gate2, linear(glu(cfg, linear(a2, w["w_gu"])), w["w_down"]))
+    return gated_residual(xr, gate2,
+                          project(cfg, glu(cfg, project(cfg, a2, w["w_gu"])), w["w_down"]))
 
 
 # --------------------------------------------------------------------------
