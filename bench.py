@@ -44,8 +44,11 @@ def parse():
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--profile-stage", default=None,
-                   help="run the seven stages of one ERNIE-shaped block once after a warm-up "
-                        "pass and exit (a small case for ncu captures)")
+                   help="run the stages of one ERNIE-shaped block once after a warm-up pass "
+                        "and exit (a small case for ncu captures); 'w8a8' runs the block's "
+                        "W8A8 stages")
+    p.add_argument("--no-w8a8", action="store_true",
+                   help="skip the W8A8-format step and block measurements")
     return p.parse_args()
 
 
@@ -269,6 +272,56 @@ def stage_breakdown(dit, wl, model, x, mod, rc, rs, reps=6):
         ("gate_up", lambda: dit.dit_linear(dit.DIT_EPI_SWIGLU, a, blk.t["w_gu"], h)),
         ("down", lambda: dit.dit_linear(dit.DIT_EPI_RESIDUAL, h, blk.t["w_down"], xs, mod[5])),
     ]
+    return time_stages(stages, reps)
+
+
+def stage_breakdown_w8a8(dit, wl, blk, x, mod, rc, rs, reps=6):
+    """Per-kernel device time of one block in the W8A8 format (8-bit e4m3
+    codes with the 256-point Hadamard rotation), each stage launched through
+    its own C-ABI entry point."""
+    import dataclasses
+
+    import torch
+    dev = x.device
+    n, H, nh, nkv, d, F = wl.n_tokens, wl.hidden, wl.n_heads, wl.n_kv_heads, wl.head_dim, wl.ffn
+    cfg = dit.block_config_from(dataclasses.replace(wl, linear_format="w8a8_h256"))
+    a8 = torch.empty(n, H, dtype=torch.uint8, device=dev)
+    sa = torch.empty(n, device=dev)
+    qk = torch.empty(nh + nkv, n, d, dtype=torch.bfloat16, device=dev)
+    vt = torch.empty(1, nkv, d, (n + 7) // 8 * 8, dtype=torch.bfloat16, device=dev)
+    o = torch.empty(n, nh * d, dtype=torch.bfloat16, device=dev)
+    o8 = torch.empty(n, nh * d, dtype=torch.uint8, device=dev)
+    so = torch.empty(n, device=dev)
+    h = torch.empty(n, F, dtype=torch.bfloat16, device=dev)
+    h8 = torch.empty(n, F, dtype=torch.uint8, device=dev)
+    sh = torch.empty(n, device=dev)
+    xs = x.clone()
+    t = blk.t
+    stages = [
+        ("ln_rotate_quantize",
+         lambda: dit.dit_ln_modulate_rotate_quantize(0, xs, mod[0], mod[1], 1e-6, a8, sa)),
+        ("qkv", lambda: dit.dit_qkv_rope_e4m3(cfg, blk, a8, sa, rc, rs, qk, vt)),
+        ("attention", lambda: dit.dit_attention(cfg, qk, vt, o)),
+        ("rotate_quantize_o", lambda: dit.dit_rotate_quantize(o, o8, so)),
+        ("out", lambda: dit.dit_linear_e4m3(dit.DIT_EPI_RESIDUAL, o8, so, t["w_o"],
+                                            t["w_o_scale"], xs, mod[2])),
+        ("ln_rotate_quantize",
+         lambda: dit.dit_ln_modulate_rotate_quantize(0, xs, mod[3], mod[4], 1e-6, a8, sa)),
+        ("gate_up", lambda: dit.dit_linear_e4m3(dit.DIT_EPI_SWIGLU, a8, sa, t["w_gu"],
+                                                t["w_gu_scale"], h)),
+        ("rotate_quantize_h", lambda: dit.dit_rotate_quantize(h, h8, sh)),
+        ("down", lambda: dit.dit_linear_e4m3(dit.DIT_EPI_RESIDUAL, h8, sh, t["w_down"],
+                                             t["w_down_scale"], xs, mod[5])),
+    ]
+    return time_stages(stages, reps)
+
+
+def time_stages(stages, reps):
+    """Runs the stages `reps` times in order with a CUDA event after each one
+    on the current stream; returns milliseconds per pass for each name (a
+    name listed twice sums both launches)."""
+    import torch
+    st = torch.cuda.current_stream()
     for _, f in stages:   # warm-up
         f()
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(len(stages) * reps + 1)]
@@ -310,7 +363,11 @@ def run_profile_stage(args):
     rs = torch.empty_like(rc)
     dit.dit_rope_table_grid(wl.grid_h, wl.grid_w, wl.n_txt, wl.rope_axes, wl.rope_theta, rc, rs)
     x = torch.randn(wl.n_tokens, wl.hidden, device=dev)
-    ms = stage_breakdown(dit, wl, model, x, mod, rc, rs, reps=1)
+    if args.profile_stage == "w8a8":
+        blk8 = dit.DeviceBlock(dict(model.blocks[0].t), dev, "w8a8_h256")
+        ms = stage_breakdown_w8a8(dit, wl, blk8, x, mod, rc, rs, reps=1)
+    else:
+        ms = stage_breakdown(dit, wl, model, x, mod, rc, rs, reps=1)
     torch.cuda.synchronize()
     assert dit.dit_last_device_error() == dit.DIT_OK
     print(json.dumps({"profile_stage": args.profile_stage, "ms_per_block": ms}), flush=True)
@@ -515,6 +572,73 @@ def run_ours(args, rank, world, local):
     del xe, ve
     hbm["peak_source"] = f"{peak_src} hbm_gbs"
 
+    # ---- the same denoiser with its projections in the W8A8 format (8-bit
+    # e4m3 codes of both operands, 256-point Hadamard rotation, per-row
+    # scales): the same weights, coded once on the GPU
+    w8a8 = None
+    if not args.no_w8a8:
+        import dataclasses
+        wl8 = dataclasses.replace(wl, linear_format="w8a8_h256")
+        cfg8 = dit.model_config_from(wl8)
+        blocks8 = [dit.DeviceBlock(dict(b.t), dev, "w8a8_h256") for b in model.blocks]
+        model8 = dit.DeviceModel(mw, dev, layers=blocks8)
+        ws8 = dit.workspace(dit.dit_denoise_workspace_bytes(cfg8, wl.grid_h, wl.grid_w,
+                                                            wl.n_txt), dev)
+        lat8 = latent0.clone()
+
+        def step8(i):
+            j = i % 8
+            dit.dit_denoise_step(cfg8, model8, lat8, text, wl.grid_h, wl.grid_w, sig[j],
+                                 sig[j + 1], ws=ws8)
+
+        for i in range(max(3, args.warmup)):
+            step8(i)
+        torch.cuda.synchronize()
+        w0, w1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        w0.record(stream)
+        for i in range(args.steps):
+            step8(i)
+        w1.record(stream)
+        torch.cuda.synchronize()
+        if dit.dit_last_device_error() != dit.DIT_OK:
+            raise RuntimeError("device error word set during the W8A8 steps")
+        ms8 = w0.elapsed_time(w1) / args.steps
+        fp8_peak = 2.0 * tc_peak
+        st8 = stage_breakdown_w8a8(dit, wl, blocks8[0], x, mod, rc, rs)
+        k8 = {}
+        n_el = wl.n_tokens
+        bytes_rq = {"ln_rotate_quantize": 2 * 5.0 * n_el * wl.hidden,    # two launches
+                    "rotate_quantize_o": 3.0 * n_el * wl.n_heads * wl.head_dim,
+                    "rotate_quantize_h": 3.0 * n_el * wl.ffn}
+        for name, ms in st8.items():
+            if name in bytes_rq:
+                gbs = bytes_rq[name] / (ms * 1e-3) / 1e9
+                k8[name] = {"ms_per_block": round(ms, 4), "bound": "hbm",
+                            "achieved": round(gbs, 1), "unit": "GB/s",
+                            "frac": round(gbs / hbm_peak, 3)}
+            else:
+                tf = per_block[name] / (ms * 1e-3) / 1e12
+                pk = tc_peak if name == "attention" else fp8_peak
+                k8[name] = {"ms_per_block": round(ms, 4), "bound": "tensor",
+                            "achieved": round(tf, 1), "unit": "TFLOP/s",
+                            "frac": round(tf / pk, 3),
+                            "dtype": "bf16" if name == "attention" else "e4m3"}
+        bws8 = dit.workspace(dit.dit_block_workspace_bytes(cfg8.block, wl.n_tokens), dev)
+        xv = x.clone()
+        ms_b8 = time_ms(lambda: dit.dit_block_forward(cfg8.block, blocks8[0], xv, mod, rc, rs,
+                                                      ws=bws8), reps=5)
+        w8a8 = {"format": "W8A8, 256-point Hadamard rotation, e4m3 codes, fp32 row scales",
+                "ms_per_step": round(ms8, 4),
+                "tflops": round(step_flops / (ms8 * 1e-3) / 1e12, 1),
+                "speedup_vs_bf16_step": round(ms_per_step_rank / ms8, 3),
+                "ms_per_block": round(ms_b8, 4),
+                "block_tflops": round(sum(per_block.values()) / (ms_b8 * 1e-3) / 1e12, 1),
+                "fp8_peak": fp8_peak,
+                "fp8_peak_source": f"{peak_src} bf16_tflops_sustained x 2 (nominal e4m3:bf16 "
+                                   f"tensor ratio)",
+                "kernels": k8}
+        del blocks8, model8, ws8, bws8
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         ms_cpu, sample, cores = cpu_oracle_sample(wl)
@@ -541,6 +665,7 @@ def run_ours(args, rank, world, local):
             "kernels": kernels,
             "hbm_kernels_large": hbm,
             "block_variants": variants,
+            "w8a8_h256": w8a8,
             "cpu_baseline": cpu,
         }
         print(json.dumps(line), flush=True)

@@ -14,7 +14,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libdit.so")
-SOURCES = ["gemm.cu", "attention.cu", "rowops.cu", "api.cu"]
+SOURCES = ["gemm.cu", "gemm_f8.cu", "attention.cu", "rowops.cu", "quant.cu", "api.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -61,9 +61,10 @@ const DeviceState* device_state() {
 
 void count_launch(int n) { t_launches += n; }
 
-bool make_tmap_bf16(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
-                    const uint64_t* strides_bytes, const uint32_t* box) {
+bool make_tmap(CUtensorMap* map, uint32_t elem_bytes, const void* base, int rank,
+               const uint64_t* dims, const uint64_t* strides_bytes, const uint32_t* box) {
   if (g_encode == nullptr || !aligned16(base)) return false;
+  if (elem_bytes != 1 && elem_bytes != 2) return false;
   cuuint64_t gd[5];
   cuuint64_t gs[4];
   cuuint32_t bx[5];
@@ -77,7 +78,10 @@ bool make_tmap_bf16(CUtensorMap* map, const void* base, int rank, const uint64_t
       gs[i] = strides_bytes[i];
     }
   }
-  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank,
+  CUresult r = g_encode(map,
+                        elem_bytes == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                        : CU_TENSOR_MAP_DATA_TYPE_UINT8,
+                        (cuuint32_t)rank,
                         const_cast<void*>(base), gd, gs, bx, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -99,11 +103,23 @@ dit_status check_block_config(const dit_block_config* c) {
   if (c->norm_kind < 0 || c->norm_kind > 1 || c->glu_act < 0 || c->glu_act > 1 ||
       c->rope_order < 0 || c->rope_order > 1 || c->gate_fn < 0 || c->gate_fn > 2)
     return DIT_EINVAL;
+  if (c->linear_format != DIT_LINEAR_BF16 && c->linear_format != DIT_LINEAR_W8A8_H256)
+    return DIT_EINVAL;
+  if (c->linear_format == DIT_LINEAR_W8A8_H256) {
+    const int hq = c->n_heads * c->head_dim;
+    if (c->hidden % 256 || hq % 256 || c->ffn % 256 || c->hidden > ROTQ_LN_MAX_H ||
+        hq > ROTQ_MAX_K || c->ffn > ROTQ_MAX_K)
+      return DIT_EUNSUPPORTED;
+  }
   return DIT_OK;
 }
 
 struct BlockWs {
   __nv_bfloat16 *a, *qk, *vt, *o, *h;
+  // W8A8 format only: e4m3 codes of the normed rows, of o and of h, and
+  // their row scales
+  uint8_t *a8, *o8, *h8;
+  float *sa, *so, *sh;
   size_t bytes;
 };
 
@@ -119,18 +135,28 @@ BlockWs block_ws_layout(const dit_block_config* c, int n_tokens, int n_seqs, voi
     off += align256(bytes);
     return reinterpret_cast<__nv_bfloat16*>(p);
   };
-  w.a = take(N * c->hidden * 2);
+  const bool q8 = c->linear_format == DIT_LINEAR_W8A8_H256;
+  w.a = take(N * c->hidden * 2);  // also the final layer's normed rows
   w.qk = take(N * (size_t)(c->n_heads + c->n_kv_heads) * hd * 2);
   w.vt = take((size_t)n_seqs * c->n_kv_heads * hd * s_pad * 2);
   w.o = take(N * (size_t)c->n_heads * hd * 2);
   w.h = take(N * (size_t)c->ffn * 2);
+  if (q8) {
+    w.a8 = reinterpret_cast<uint8_t*>(take(N * c->hidden));
+    w.o8 = reinterpret_cast<uint8_t*>(take(N * (size_t)c->n_heads * hd));
+    w.h8 = reinterpret_cast<uint8_t*>(take(N * (size_t)c->ffn));
+    w.sa = reinterpret_cast<float*>(take(N * 4));
+    w.so = reinterpret_cast<float*>(take(N * 4));
+    w.sh = reinterpret_cast<float*>(take(N * 4));
+  }
   w.bytes = off;
   return w;
 }
 
+// a: bf16 rows, or e4m3 codes with row scales a_scale (W8A8 format).
 dit_status run_qkv(const dit_block_config* c, const dit_block_weights* w, const void* a,
-                   int n_tokens, int n_seqs, const float* rc, const float* rs,
-                   __nv_bfloat16* qk, __nv_bfloat16* vt, cudaStream_t st) {
+                   const float* a_scale, int n_tokens, int n_seqs, const float* rc,
+                   const float* rs, __nv_bfloat16* qk, __nv_bfloat16* vt, cudaStream_t st) {
   const int hd = c->head_dim;
   GemmParams p{};
   p.M = n_tokens;
@@ -154,7 +180,24 @@ dit_status run_qkv(const dit_block_config* c, const dit_block_weights* w, const 
   p.qkv.rms = c->norm_kind;
   p.qkv.rope_first = c->rope_order;
   p.qkv.eps = c->ln_eps;
+  if (a_scale) {
+    p.sa = a_scale;
+    p.sb = w->w_qkv_scale;
+    return cuda_status(launch_gemm_f8(EPI_QKV, hd, a, c->hidden, w->w_qkv, c->hidden, p, st));
+  }
   return cuda_status(launch_gemm(EPI_QKV, hd, a, c->hidden, w->w_qkv, c->hidden, p, st));
+}
+
+// One projection of the block: bf16 operands, or e4m3 codes with row scales
+// sa (activations) and sb (weights) when sa is set.
+cudaError_t project(int epi, const void* A, const float* sa, long long lda, const void* B,
+                    const float* sb, long long ldb, GemmParams& p, cudaStream_t st) {
+  if (sa) {
+    p.sa = sa;
+    p.sb = sb;
+    return launch_gemm_f8(epi, 0, A, lda, B, ldb, p, st);
+  }
+  return launch_gemm(epi, 0, A, lda, B, ldb, p, st);
 }
 
 int residual_epi(int gate_fn) {
@@ -164,31 +207,41 @@ int residual_epi(int gate_fn) {
 dit_status block_forward_impl(const dit_block_config* c, const dit_block_weights* w, float* x,
                               int n_tokens, int n_seqs, const float* mod, const float* rc,
                               const float* rs, const BlockWs& ws, cudaStream_t st) {
-  const int H = c->hidden, hd = c->head_dim, F = c->ffn;
+  const int H = c->hidden, hd = c->head_dim, F = c->ffn, HQ = c->n_heads * c->head_dim;
   const bool ada = c->adaln != 0;
+  const bool q8 = c->linear_format == DIT_LINEAR_W8A8_H256;
   const int ln_mode = (ada ? 0 : 1) | (c->norm_kind ? 2 : 0);
   cudaError_t e;
   // a = norm(x) (1 + scale1) + shift1   |   norm(x) g1 + b1
-  e = launch_ln_modulate(ln_mode, x, H, n_tokens, H, ada ? mod : w->ln1_g,
-                         ada ? mod + H : w->ln1_b, c->ln_eps, ws.a, H, st);
+  // (W8A8: rotated and coded in the same kernel, never stored in bf16)
+  auto norm_rows = [&](const float* p0, const float* p1) {
+    return q8 ? launch_ln_rotate_quant(ln_mode, x, H, n_tokens, H, p0, p1, c->ln_eps, ws.a8, H,
+                                       ws.sa, st)
+              : launch_ln_modulate(ln_mode, x, H, n_tokens, H, p0, p1, c->ln_eps, ws.a, H, st);
+  };
+  const void* a_op = q8 ? static_cast<const void*>(ws.a8) : ws.a;
+  e = norm_rows(ada ? mod : w->ln1_g, ada ? mod + H : w->ln1_b);
   if (e != cudaSuccess) return DIT_ECUDA;
-  dit_status s = run_qkv(c, w, ws.a, n_tokens, n_seqs, rc, rs, ws.qk, ws.vt, st);
+  dit_status s = run_qkv(c, w, a_op, q8 ? ws.sa : nullptr, n_tokens, n_seqs, rc, rs, ws.qk,
+                         ws.vt, st);
   if (s != DIT_OK) return s;
   e = launch_attention(hd, ws.qk, ws.vt, n_tokens, n_seqs, c->n_heads, c->n_kv_heads, ws.o, st);
   if (e != cudaSuccess) return DIT_ECUDA;
+  if (q8 && launch_rotate_quant(ws.o, HQ, n_tokens, HQ, ws.o8, HQ, ws.so, st) != cudaSuccess)
+    return DIT_ECUDA;
   {  // x += gate1 (o Wo^T)
     GemmParams p{};
     p.M = n_tokens;
     p.N = H;
-    p.K = c->n_heads * hd;
+    p.K = HQ;
     p.out = x;
     p.ldo = H;
     p.vec = ada ? mod + 2 * H : nullptr;
-    e = launch_gemm(residual_epi(ada ? c->gate_fn : 0), 0, ws.o, p.K, w->w_o, p.K, p, st);
+    e = project(residual_epi(ada ? c->gate_fn : 0), q8 ? (const void*)ws.o8 : ws.o,
+                q8 ? ws.so : nullptr, HQ, w->w_o, w->w_o_scale, HQ, p, st);
     if (e != cudaSuccess) return DIT_ECUDA;
   }
-  e = launch_ln_modulate(ln_mode, x, H, n_tokens, H, ada ? mod + 3 * H : w->ln2_g,
-                         ada ? mod + 4 * H : w->ln2_b, c->ln_eps, ws.a, H, st);
+  e = norm_rows(ada ? mod + 3 * H : w->ln2_g, ada ? mod + 4 * H : w->ln2_b);
   if (e != cudaSuccess) return DIT_ECUDA;
   {  // h = SiLU(a Wg^T) (a Wu^T)
     GemmParams p{};
@@ -197,9 +250,12 @@ dit_status block_forward_impl(const dit_block_config* c, const dit_block_weights
     p.K = H;
     p.out = ws.h;
     p.ldo = F;
-    e = launch_gemm(c->glu_act ? EPI_GEGLU : EPI_SWIGLU, 0, ws.a, H, w->w_gu, H, p, st);
+    e = project(c->glu_act ? EPI_GEGLU : EPI_SWIGLU, a_op, q8 ? ws.sa : nullptr, H, w->w_gu,
+                w->w_gu_scale, H, p, st);
     if (e != cudaSuccess) return DIT_ECUDA;
   }
+  if (q8 && launch_rotate_quant(ws.h, F, n_tokens, F, ws.h8, F, ws.sh, st) != cudaSuccess)
+    return DIT_ECUDA;
   {  // x += gate2 (h Wd^T)
     GemmParams p{};
     p.M = n_tokens;
@@ -208,7 +264,8 @@ dit_status block_forward_impl(const dit_block_config* c, const dit_block_weights
     p.out = x;
     p.ldo = H;
     p.vec = ada ? mod + 5 * H : nullptr;
-    e = launch_gemm(residual_epi(ada ? c->gate_fn : 0), 0, ws.h, F, w->w_down, F, p, st);
+    e = project(residual_epi(ada ? c->gate_fn : 0), q8 ? (const void*)ws.h8 : ws.h,
+                q8 ? ws.sh : nullptr, F, w->w_down, w->w_down_scale, F, p, st);
     if (e != cudaSuccess) return DIT_ECUDA;
   }
   return DIT_OK;
@@ -218,6 +275,11 @@ dit_status check_block_weights(const dit_block_config* c, const dit_block_weight
   if (!w || !w->w_qkv || !w->w_o || !w->w_gu || !w->w_down) return DIT_EINVAL;
   if (!aligned16(w->w_qkv) || !aligned16(w->w_o) || !aligned16(w->w_gu) || !aligned16(w->w_down))
     return DIT_EINVAL;
+  if (c->linear_format == DIT_LINEAR_W8A8_H256) {
+    const float* sc[4] = {w->w_qkv_scale, w->w_o_scale, w->w_gu_scale, w->w_down_scale};
+    for (const float* p : sc)
+      if (!p || !aligned16(p)) return DIT_EINVAL;
+  }
   if (c->qk_norm && (!w->q_g || !w->q_b || !w->k_g || !w->k_b)) return DIT_EINVAL;
   if (!c->adaln) {
     if (!w->ln1_g || !w->ln1_b || !w->ln2_g || !w->ln2_b) return DIT_EINVAL;
@@ -503,6 +565,72 @@ dit_status dit_linear(int32_t epilogue, const void* a, int64_t lda, const void* 
   return cuda_status(launch_gemm(kind, 0, a, lda, w, ldw, p, static_cast<cudaStream_t>(stream)));
 }
 
+dit_status dit_linear_e4m3(int32_t epilogue, const void* a, const float* a_scales, int64_t lda,
+                           const void* w, const float* w_scales, int64_t ldw, int32_t M,
+                           int32_t N, int32_t K, void* out, int64_t ldo,
+                           const float* bias_or_gate, void* stream) {
+  if (epilogue < DIT_EPI_BF16 || epilogue > DIT_EPI_RESIDUAL_SIGMOID) return DIT_EINVAL;
+  if (!a || !w || !out || !a_scales || !w_scales || M <= 0 || N <= 0 || K <= 0)
+    return DIT_EINVAL;
+  if (K % 16 || lda < K || ldw < K || lda % 16 || ldw % 16) return DIT_EINVAL;
+  if (!aligned16(a) || !aligned16(w) || !aligned16(out) || !aligned16(w_scales) ||
+      (reinterpret_cast<uintptr_t>(a_scales) & 3u))
+    return DIT_EINVAL;
+  if (bias_or_gate && !aligned16(bias_or_gate)) return DIT_EINVAL;
+  const bool glu = epilogue == DIT_EPI_SWIGLU || epilogue == DIT_EPI_GEGLU;
+  const bool resid = epilogue == DIT_EPI_RESIDUAL || epilogue == DIT_EPI_RESIDUAL_TANH ||
+                     epilogue == DIT_EPI_RESIDUAL_SIGMOID;
+  const bool f32_out = epilogue == DIT_EPI_F32_BIAS || resid;
+  if (ldo < N || ldo % (f32_out ? 4 : 8)) return DIT_EINVAL;
+  if (glu && N % 128) return DIT_EUNSUPPORTED;
+  if (!device_state()) return DIT_ECUDA;
+  GemmParams p{};
+  p.M = M;
+  p.N = N;
+  p.K = K;
+  p.out = out;
+  p.ldo = ldo;
+  p.vec = glu ? nullptr : bias_or_gate;
+  p.sa = a_scales;
+  p.sb = w_scales;
+  const int kind = epilogue == DIT_EPI_GEGLU            ? EPI_GEGLU
+                   : epilogue == DIT_EPI_RESIDUAL_TANH    ? EPI_RESIDUAL_TANH
+                   : epilogue == DIT_EPI_RESIDUAL_SIGMOID ? EPI_RESIDUAL_SIGMOID
+                                                          : epilogue;
+  return cuda_status(
+      launch_gemm_f8(kind, 0, a, lda, w, ldw, p, static_cast<cudaStream_t>(stream)));
+}
+
+dit_status dit_rotate_quantize(const void* x, int64_t ldx, int32_t rows, int32_t K, void* codes,
+                               int64_t ldq, float* scales, void* stream) {
+  if (!x || !codes || !scales || rows < 0 || K <= 0) return DIT_EINVAL;
+  if (K % 256 || ldx < K || ldq < K || ldx % 8 || ldq % 16 || !aligned16(x) ||
+      !aligned16(codes) || (reinterpret_cast<uintptr_t>(scales) & 3u))
+    return DIT_EINVAL;
+  if (K > ROTQ_MAX_K) return DIT_EUNSUPPORTED;
+  if (!device_state()) return DIT_ECUDA;
+  return cuda_status(launch_rotate_quant(static_cast<const __nv_bfloat16*>(x), ldx, rows, K,
+                                         static_cast<uint8_t*>(codes), ldq, scales,
+                                         static_cast<cudaStream_t>(stream)));
+}
+
+dit_status dit_ln_modulate_rotate_quantize(int32_t mode, const float* x, int64_t ldx,
+                                           int32_t rows, int32_t H, const float* p0,
+                                           const float* p1, float eps, void* codes,
+                                           int64_t ldq, float* scales, void* stream) {
+  if (mode < 0 || mode > 3 || !x || !p0 || !p1 || !codes || !scales || rows < 0 || H <= 0)
+    return DIT_EINVAL;
+  if (H % 256 || ldx < H || ldq < H || ldx % 4 || ldq % 16 || !aligned16(x) ||
+      !aligned16(p0) || !aligned16(p1) || !aligned16(codes) ||
+      (reinterpret_cast<uintptr_t>(scales) & 3u) || !(eps >= 0.0f))
+    return DIT_EINVAL;
+  if (H > ROTQ_LN_MAX_H) return DIT_EUNSUPPORTED;
+  if (!device_state()) return DIT_ECUDA;
+  return cuda_status(launch_ln_rotate_quant(mode, x, ldx, rows, H, p0, p1, eps,
+                                            static_cast<uint8_t*>(codes), ldq, scales,
+                                            static_cast<cudaStream_t>(stream)));
+}
+
 dit_status dit_qkv_rope(const dit_block_config* cfg, const dit_block_weights* w, const void* a,
                         int32_t n_tokens, int32_t n_seqs, const float* rope_cos,
                         const float* rope_sin, void* qk, void* vt, void* stream) {
@@ -516,8 +644,31 @@ dit_status dit_qkv_rope(const dit_block_config* cfg, const dit_block_weights* w,
   if (!aligned16(a) || !aligned16(qk) || !aligned16(vt) || !aligned16(rope_cos) ||
       !aligned16(rope_sin))
     return DIT_EINVAL;
+  if (cfg->linear_format != DIT_LINEAR_BF16) return DIT_EUNSUPPORTED;
   if (!device_state()) return DIT_ECUDA;
-  return run_qkv(cfg, w, a, n_tokens, n_seqs, rope_cos, rope_sin,
+  return run_qkv(cfg, w, a, nullptr, n_tokens, n_seqs, rope_cos, rope_sin,
+                 static_cast<__nv_bfloat16*>(qk), static_cast<__nv_bfloat16*>(vt),
+                 static_cast<cudaStream_t>(stream));
+}
+
+dit_status dit_qkv_rope_e4m3(const dit_block_config* cfg, const dit_block_weights* w,
+                             const void* a, const float* a_scales, int32_t n_tokens,
+                             int32_t n_seqs, const float* rope_cos, const float* rope_sin,
+                             void* qk, void* vt, void* stream) {
+  dit_status s = check_block_config(cfg);
+  if (s != DIT_OK) return s;
+  if (cfg->linear_format != DIT_LINEAR_W8A8_H256) return DIT_EINVAL;
+  if (!w || !w->w_qkv || !aligned16(w->w_qkv) || !w->w_qkv_scale || !aligned16(w->w_qkv_scale))
+    return DIT_EINVAL;
+  if (cfg->qk_norm && (!w->q_g || !w->q_b || !w->k_g || !w->k_b)) return DIT_EINVAL;
+  if (!a || !a_scales || !qk || !vt || !rope_cos || !rope_sin || n_tokens <= 0 || n_seqs <= 0 ||
+      n_tokens % n_seqs)
+    return DIT_EINVAL;
+  if (!aligned16(a) || !aligned16(qk) || !aligned16(vt) || !aligned16(rope_cos) ||
+      !aligned16(rope_sin) || (reinterpret_cast<uintptr_t>(a_scales) & 3u))
+    return DIT_EINVAL;
+  if (!device_state()) return DIT_ECUDA;
+  return run_qkv(cfg, w, a, a_scales, n_tokens, n_seqs, rope_cos, rope_sin,
                  static_cast<__nv_bfloat16*>(qk), static_cast<__nv_bfloat16*>(vt),
                  static_cast<cudaStream_t>(stream));
 }

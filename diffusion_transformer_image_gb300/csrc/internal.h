@@ -21,10 +21,15 @@ const DeviceState* device_state();  // nullptr if CUDA is unusable
 inline DevErr dev_err(const DeviceState* ds) { return DevErr{ds->err, ds->timeout_ns}; }
 void count_launch(int n = 1);
 
-// Encodes a row-major bf16 tensor map with 128-byte swizzle.
+// Encodes a row-major tensor map with 128-byte swizzle: bf16 elements
+// (elem_bytes 2) or bytes (elem_bytes 1, the e4m3 codes).
 // dims[0] is the contiguous dimension; strides_bytes has rank-1 entries.
-bool make_tmap_bf16(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
-                    const uint64_t* strides_bytes, const uint32_t* box);
+bool make_tmap(CUtensorMap* map, uint32_t elem_bytes, const void* base, int rank,
+               const uint64_t* dims, const uint64_t* strides_bytes, const uint32_t* box);
+inline bool make_tmap_bf16(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
+                           const uint64_t* strides_bytes, const uint32_t* box) {
+  return make_tmap(map, 2, base, rank, dims, strides_bytes, box);
+}
 
 // ------------------------------------------------------------------ GEMM
 enum GemmEpi : int {
@@ -57,6 +62,8 @@ struct GemmParams {
   void* out;
   long long ldo;
   const float* vec;     // bias (EPI_F32_BIAS) or gate (EPI_RESIDUAL), may be null
+  const float* sa;      // e4m3 GEMM: scale of each A row [M]
+  const float* sb;      // e4m3 GEMM: scale of each B row [N] (GLU: [2N])
   QkvEpi qkv;
   DevErr err;
 };
@@ -65,6 +72,10 @@ struct GemmParams {
 // width (64 or 128).  Returns cudaSuccess or the launch error.
 cudaError_t launch_gemm(int epi, int hd, const void* A, long long lda, const void* B,
                         long long ldb, GemmParams& p, cudaStream_t st);
+// The same with e4m3 codes for A and B (lda, ldb in elements = bytes) and the
+// row scales p.sa, p.sb applied to the accumulator before the epilogue.
+cudaError_t launch_gemm_f8(int epi, int hd, const void* A, long long lda, const void* B,
+                           long long ldb, GemmParams& p, cudaStream_t st);
 
 // ------------------------------------------------------------- attention
 cudaError_t launch_attention(int hd, const __nv_bfloat16* qk, const __nv_bfloat16* vt,
@@ -77,6 +88,18 @@ cudaError_t launch_ln_modulate(int mode, const float* x, long long ldx, int rows
                                const float* p0, const float* p1, float eps,
                                __nv_bfloat16* out, long long ldo, cudaStream_t st,
                                __nv_bfloat16* out_lo = nullptr);
+// W8A8 coding ([ZFLOW] section VII): rows rotated by the 256-point Hadamard
+// matrix along K, then e4m3 codes with one fp32 scale per row.  K (or H) a
+// multiple of 256; codes [rows, ldq] bytes, scale [rows].
+constexpr int ROTQ_MAX_K = 16384;
+constexpr int ROTQ_LN_MAX_H = 8192;
+cudaError_t launch_rotate_quant(const __nv_bfloat16* x, long long ldx, int rows, int K,
+                                uint8_t* q, long long ldq, float* scale, cudaStream_t st);
+// The same applied to launch_ln_modulate's output (same mode bits), which is
+// never written in bf16.
+cudaError_t launch_ln_rotate_quant(int mode, const float* x, long long ldx, int rows, int H,
+                                   const float* p0, const float* p1, float eps, uint8_t* q,
+                                   long long ldq, float* scale, cudaStream_t st);
 cudaError_t launch_euler(float* x, const float* v, long long n, float dt, cudaStream_t st);
 cudaError_t launch_gemv(const __nv_bfloat16* W, const float* x, const float* b, float* y,
                         int O, int K, int silu_in, cudaStream_t st);

@@ -34,11 +34,14 @@ NORM_KINDS = {"layer": 0, "rms": 1}
 GLU_ACTS = {"silu": 0, "gelu_tanh": 1}
 ROPE_ORDERS = {"norm_rope": 0, "rope_norm": 1}
 GATE_FNS = {"identity": 0, "tanh": 1, "sigmoid": 2}
+LINEAR_FORMATS = {"bf16": 0, "w8a8_h256": 1}
 
 EXPORTED = [
     "dit_block_workspace_bytes", "dit_block_forward", "dit_denoise_workspace_bytes",
     "dit_denoise_step", "flowmatch_euler_step", "flowmatch_sigmas", "dit_linear",
-    "dit_qkv_rope", "dit_attention", "dit_ln_modulate", "dit_timestep_conditioning",
+    "dit_qkv_rope", "dit_qkv_rope_e4m3", "dit_attention", "dit_ln_modulate",
+    "dit_rotate_quantize", "dit_ln_modulate_rotate_quantize", "dit_linear_e4m3",
+    "dit_timestep_conditioning",
     "dit_timestep_conditioning_noalloc",
     "dit_rope_table_grid", "dit_rope_table_pos", "dit_rope_table_vit",
     "dit_last_device_error", "dit_set_wait_timeout_ns", "dit_debug_stuck_wait",
@@ -57,12 +60,14 @@ class BlockConfig(ctypes.Structure):
                 ("head_dim", c_int32), ("ffn", c_int32), ("rope_layout", c_int32),
                 ("adaln", c_int32), ("qk_norm", c_int32), ("ln_eps", c_float),
                 ("norm_kind", c_int32), ("glu_act", c_int32), ("rope_order", c_int32),
-                ("gate_fn", c_int32)]
+                ("gate_fn", c_int32), ("linear_format", c_int32)]
 
 
 class BlockWeights(ctypes.Structure):
     _fields_ = [(n, c_void_p) for n in ("w_qkv", "w_o", "w_gu", "w_down", "q_g", "q_b", "k_g",
-                                        "k_b", "ln1_g", "ln1_b", "ln2_g", "ln2_b")]
+                                        "k_b", "ln1_g", "ln1_b", "ln2_g", "ln2_b",
+                                        "w_qkv_scale", "w_o_scale", "w_gu_scale",
+                                        "w_down_scale")]
 
 
 class ModelConfig(ctypes.Structure):
@@ -99,10 +104,21 @@ _sig("dit_linear", c_int32, [c_int32, c_void_p, c_int64, c_void_p, c_int64, c_in
                              c_int32, c_void_p, c_int64, c_void_p, c_void_p])
 _sig("dit_qkv_rope", c_int32, [_P(BlockConfig), _P(BlockWeights), c_void_p, c_int32, c_int32,
                                c_void_p, c_void_p, c_void_p, c_void_p, c_void_p])
+_sig("dit_qkv_rope_e4m3", c_int32, [_P(BlockConfig), _P(BlockWeights), c_void_p, c_void_p,
+                                    c_int32, c_int32, c_void_p, c_void_p, c_void_p, c_void_p,
+                                    c_void_p])
 _sig("dit_attention", c_int32, [_P(BlockConfig), c_void_p, c_void_p, c_int32, c_int32, c_void_p,
                                 c_void_p])
 _sig("dit_ln_modulate", c_int32, [c_int32, c_void_p, c_int64, c_int32, c_int32, c_void_p, c_void_p,
                                   c_float, c_void_p, c_void_p])
+_sig("dit_rotate_quantize", c_int32, [c_void_p, c_int64, c_int32, c_int32, c_void_p, c_int64,
+                                      c_void_p, c_void_p])
+_sig("dit_ln_modulate_rotate_quantize", c_int32, [c_int32, c_void_p, c_int64, c_int32, c_int32,
+                                                  c_void_p, c_void_p, c_float, c_void_p, c_int64,
+                                                  c_void_p, c_void_p])
+_sig("dit_linear_e4m3", c_int32, [c_int32, c_void_p, c_void_p, c_int64, c_void_p, c_void_p,
+                                  c_int64, c_int32, c_int32, c_int32, c_void_p, c_int64, c_void_p,
+                                  c_void_p])
 _sig("dit_timestep_conditioning", c_int32, [_P(ModelConfig), _P(ModelWeights), c_float, c_void_p,
                                             c_void_p, c_void_p, c_void_p])
 _sig("dit_timestep_conditioning_noalloc", c_int32, [_P(ModelConfig), _P(ModelWeights), c_float,
@@ -142,18 +158,21 @@ def _stream(stream=None):
 # --------------------------------------------------------------- structures
 def block_config(hidden, n_heads, n_kv_heads, head_dim, ffn, rope_layout="interleaved",
                  adaln=True, qk_norm=True, ln_eps=1e-6, norm_kind="layer", glu="silu",
-                 rope_order="norm_rope", gate_fn="identity") -> BlockConfig:
+                 rope_order="norm_rope", gate_fn="identity",
+                 linear_format="bf16") -> BlockConfig:
     return BlockConfig(hidden, n_heads, n_kv_heads, head_dim, ffn,
                        0 if rope_layout == "interleaved" else 1, int(bool(adaln)),
                        int(bool(qk_norm)), ln_eps, NORM_KINDS[norm_kind], GLU_ACTS[glu],
-                       ROPE_ORDERS[rope_order], GATE_FNS[gate_fn])
+                       ROPE_ORDERS[rope_order], GATE_FNS[gate_fn],
+                       LINEAR_FORMATS[linear_format])
 
 
 def block_config_from(wl) -> BlockConfig:
     """BlockConfig of a synthetic workload description (synth.Workload)."""
     return block_config(wl.hidden, wl.n_heads, wl.n_kv_heads, wl.head_dim, wl.ffn,
                         wl.rope_layout, wl.adaln, wl.qk_norm, norm_kind=wl.norm_kind,
-                        glu=wl.glu, rope_order=wl.rope_order, gate_fn=wl.gate_fn)
+                        glu=wl.glu, rope_order=wl.rope_order, gate_fn=wl.gate_fn,
+                        linear_format=wl.linear_format)
 
 
 def model_config_from(wl, n_layers: Optional[int] = None) -> ModelConfig:
@@ -168,16 +187,27 @@ def model_config_from(wl, n_layers: Optional[int] = None) -> ModelConfig:
     return m
 
 
+LINEAR_KEYS = ("w_qkv", "w_o", "w_gu", "w_down")
+
+
 class DeviceBlock:
     """One block's weights resident on the GPU, with the C structure that
-    points at them (the tensors are kept alive by this object)."""
+    points at them (the tensors are kept alive by this object).  With
+    linear_format "w8a8_h256" the four projection weights are rotated and
+    coded on the GPU (dit_rotate_quantize) and only the codes and their row
+    scales are kept."""
 
-    def __init__(self, w: dict, device="cuda"):
+    def __init__(self, w: dict, device="cuda", linear_format: str = "bf16"):
         def dev(t, dtype):
             return None if t is None else t.to(device=device, dtype=dtype).contiguous()
-        self.t = {k: dev(w.get(k), torch.bfloat16) for k in ("w_qkv", "w_o", "w_gu", "w_down")}
+        self.t = {k: dev(w.get(k), torch.bfloat16) for k in LINEAR_KEYS}
         for k in ("q_g", "q_b", "k_g", "k_b", "ln1_g", "ln1_b", "ln2_g", "ln2_b"):
             self.t[k] = dev(w.get(k), torch.float32)
+        for k in LINEAR_KEYS:
+            self.t[k + "_scale"] = None
+        if LINEAR_FORMATS[linear_format] == LINEAR_FORMATS["w8a8_h256"]:
+            for k in LINEAR_KEYS:
+                self.t[k], self.t[k + "_scale"] = dit_rotate_quantize(self.t[k])
         self.c = BlockWeights(*[(None if self.t[n] is None else self.t[n].data_ptr())
                                 for n, _ in BlockWeights._fields_])
 
@@ -185,13 +215,14 @@ class DeviceBlock:
 class DeviceModel:
     """Denoiser weights resident on the GPU."""
 
-    def __init__(self, mw: dict, device="cuda", layers=None):
+    def __init__(self, mw: dict, device="cuda", layers=None, linear_format: str = "bf16"):
         self.t = {}
         for k in ("patch_w", "t_w1", "t_w2", "mod_w", "fin_w", "out_w"):
             self.t[k] = mw[k].to(device=device, dtype=torch.bfloat16).contiguous()
         for k in ("patch_b", "t_b1", "t_b2", "mod_b", "fin_b", "out_b"):
             self.t[k] = mw[k].to(device=device, dtype=torch.float32).contiguous()
-        self.blocks = layers if layers is not None else [DeviceBlock(l, device) for l in mw["layers"]]
+        self.blocks = layers if layers is not None else [
+            DeviceBlock(l, device, linear_format) for l in mw["layers"]]
         self.layer_array = (BlockWeights * max(1, len(self.blocks)))(*[b.c for b in self.blocks])
         self.c = ModelWeights(*[self.t[n].data_ptr() for n, _ in ModelWeights._fields_[:-1]])
         self.c.layers = ctypes.cast(self.layer_array, ctypes.POINTER(BlockWeights))
@@ -264,6 +295,13 @@ def dit_qkv_rope(cfg: BlockConfig, w: DeviceBlock, a, rope_cos, rope_sin, qk, vt
            "dit_qkv_rope")
 
 
+def dit_qkv_rope_e4m3(cfg: BlockConfig, w: DeviceBlock, a, a_scales, rope_cos, rope_sin, qk, vt,
+                      n_seqs=1, stream=None):
+    _check(lib.dit_qkv_rope_e4m3(ctypes.byref(cfg), ctypes.byref(w.c), _ptr(a), _ptr(a_scales),
+                                 a.shape[0], n_seqs, _ptr(rope_cos), _ptr(rope_sin), _ptr(qk),
+                                 _ptr(vt), _stream(stream)), "dit_qkv_rope_e4m3")
+
+
 def dit_attention(cfg: BlockConfig, qk, vt, o, n_seqs=1, stream=None):
     """qk: [n_heads + n_kv_heads, n_tokens, d] bf16 (head-major); vt as written
     by dit_qkv_rope; o: [n_tokens, n_heads * d] bf16."""
@@ -277,6 +315,43 @@ def dit_ln_modulate(mode: int, x: torch.Tensor, p0, p1, eps: float, out: torch.T
     rows, H = x.shape
     _check(lib.dit_ln_modulate(mode, _ptr(x), x.stride(0), rows, H, _ptr(p0), _ptr(p1), eps,
                                _ptr(out), _stream(stream)), "dit_ln_modulate")
+    return out
+
+
+def dit_rotate_quantize(x: torch.Tensor, codes: Optional[torch.Tensor] = None,
+                        scales: Optional[torch.Tensor] = None, stream=None):
+    """Rows of bf16 x [rows, K] rotated by the 256-point Hadamard matrix and
+    coded in e4m3: returns (codes uint8 [rows, K], scales fp32 [rows])."""
+    rows, K = x.shape
+    if codes is None:
+        codes = torch.empty(rows, K, dtype=torch.uint8, device=x.device)
+    if scales is None:
+        scales = torch.empty(rows, dtype=torch.float32, device=x.device)
+    _check(lib.dit_rotate_quantize(_ptr(x), x.stride(0), rows, K, _ptr(codes), codes.stride(0),
+                                   _ptr(scales), _stream(stream)), "dit_rotate_quantize")
+    return codes, scales
+
+
+def dit_ln_modulate_rotate_quantize(mode: int, x: torch.Tensor, p0, p1, eps: float,
+                                    codes: torch.Tensor, scales: torch.Tensor, stream=None):
+    rows, H = x.shape
+    _check(lib.dit_ln_modulate_rotate_quantize(mode, _ptr(x), x.stride(0), rows, H, _ptr(p0),
+                                               _ptr(p1), eps, _ptr(codes), codes.stride(0),
+                                               _ptr(scales), _stream(stream)),
+           "dit_ln_modulate_rotate_quantize")
+    return codes, scales
+
+
+def dit_linear_e4m3(epilogue: int, a: torch.Tensor, a_scales: torch.Tensor, w: torch.Tensor,
+                    w_scales: torch.Tensor, out: torch.Tensor, bias_or_gate=None,
+                    n_out: Optional[int] = None, stream=None):
+    """dit_linear on e4m3 codes (uint8 tensors) with per-row scales."""
+    M, K = a.shape
+    glu = epilogue in (DIT_EPI_SWIGLU, DIT_EPI_GEGLU)
+    N = n_out if n_out is not None else (w.shape[0] // 2 if glu else w.shape[0])
+    _check(lib.dit_linear_e4m3(epilogue, _ptr(a), _ptr(a_scales), a.stride(0), _ptr(w),
+                               _ptr(w_scales), w.stride(0), M, N, K, _ptr(out), out.stride(0),
+                               _ptr(bias_or_gate), _stream(stream)), "dit_linear_e4m3")
     return out
 
 

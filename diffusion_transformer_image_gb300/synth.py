@@ -48,6 +48,7 @@ class Workload:
     glu: str = "silu"
     rope_order: str = "norm_rope"
     gate_fn: str = "identity"
+    linear_format: str = "bf16"  # or "w8a8_h256" (the projections' 8-bit format)
 
     @property
     def seq_len(self) -> int:

@@ -22,7 +22,9 @@
  *     aligned and every row stride a multiple of 16 bytes (the tensor-memory
  *     copy engine requires it); violations return DIT_EINVAL.
  *   - Matrices are row-major.  Weights are bf16 and stored [out, in], so a
- *     linear computes y = x W^T.
+ *     linear computes y = x W^T.  In the W8A8 format (linear_format 1) the
+ *     four projection weights are instead e4m3 codes of the rotated weights
+ *     with one fp32 scale per row, made by dit_rotate_quantize.
  *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  All
  *     work is enqueued asynchronously on it.
  *   - Errors: invalid arguments return DIT_EINVAL and enqueue nothing; shapes
@@ -71,7 +73,16 @@ typedef struct {
                            argument clamped to +-20 and the output to +-65504 */
   int32_t rope_order;   /* [0] qk-norm then RoPE; 1 RoPE then qk-norm */
   int32_t gate_fn;      /* [0] x + g y; 1 x + tanh(g) y; 2 x + sigmoid(g) y */
+  /* Format of the four projections ([ZFLOW] section VII, "W8A8Rot"):
+   * [0] bf16 operands; 1 W8A8 with the H256 rotation: the activation rows
+   * are rotated along K by the 256-point Hadamard matrix and coded in e4m3
+   * with one scale per row inside the block, the weights arrive already
+   * rotated and coded (dit_rotate_quantize).  Needs hidden, n_heads d and
+   * ffn to be multiples of 256. */
+  int32_t linear_format;
 } dit_block_config;
+
+enum { DIT_LINEAR_BF16 = 0, DIT_LINEAR_W8A8_H256 = 1 };
 
 /* One block's weights, all device pointers.  Linears bf16 [out, in]:
  *   w_qkv  [(n_heads + 2 n_kv_heads) d, H]  rows: q heads, k heads, v heads
@@ -79,11 +90,16 @@ typedef struct {
  *   w_gu   [2F, H]   gate rows first, then up rows
  *   w_down [H, F]
  * Norm parameters fp32: q_g, q_b, k_g, k_b [d] (used when qk_norm);
- * ln1_g, ln1_b, ln2_g, ln2_b [H] (used when adaln == 0). */
+ * ln1_g, ln1_b, ln2_g, ln2_b [H] (used when adaln == 0).
+ * With linear_format DIT_LINEAR_W8A8_H256 the four linears hold e4m3 codes
+ * (one byte per element, same shapes) of the rotated weights and the four
+ * scale pointers their fp32 per-row scales [rows]; otherwise the scales are
+ * ignored. */
 typedef struct {
   const void *w_qkv, *w_o, *w_gu, *w_down;
   const float *q_g, *q_b, *k_g, *k_b;
   const float *ln1_g, *ln1_b, *ln2_g, *ln2_b;
+  const float *w_qkv_scale, *w_o_scale, *w_gu_scale, *w_down_scale;
 } dit_block_weights;
 
 /* The denoiser around the blocks ([ERNIE] section IV: latent [4096,128] ->
@@ -216,6 +232,16 @@ dit_status dit_qkv_rope(const dit_block_config* cfg, const dit_block_weights* w,
                         const float* rope_cos, const float* rope_sin, void* qk,
                         void* vt, void* stream);
 
+/* dit_qkv_rope in the W8A8 format (cfg->linear_format == 1): a holds e4m3
+ * codes [n_tokens, H] of the rotated normed rows (dit_ln_modulate_rotate_
+ * quantize) with row scales a_scales [n_tokens]; w->w_qkv holds the rotated
+ * weight's codes and w->w_qkv_scale their row scales.  Outputs as
+ * dit_qkv_rope. */
+dit_status dit_qkv_rope_e4m3(const dit_block_config* cfg, const dit_block_weights* w,
+                             const void* a, const float* a_scales, int32_t n_tokens,
+                             int32_t n_seqs, const float* rope_cos, const float* rope_sin,
+                             void* qk, void* vt, void* stream);
+
 /* Non-causal attention per sequence ([ERNIE] section VII, Decision 2: no
  * mask) with grouped KV heads ([ZFLOW] section VI, attention(heads,
  * kv_heads)): o_h = softmax(q_h k_g^T / sqrt(d)) v_g, g = h / (n_heads /
@@ -233,6 +259,39 @@ dit_status dit_attention(const dit_block_config* cfg, const void* qk, const void
 dit_status dit_ln_modulate(int32_t mode, const float* x, int64_t ldx, int32_t rows,
                            int32_t H, const float* p0, const float* p1, float eps,
                            void* out, void* stream);
+
+/* W8A8 coding of the rows of a bf16 matrix ([ZFLOW] section VII: 8-bit codes
+ * per row, H256 rotation on both sides, exact in real arithmetic because
+ * (x H)(W H)^T = x W^T for orthogonal H).  Each row is multiplied, in
+ * independent blocks of 256 columns, by the 256-point Sylvester Hadamard
+ * matrix scaled by 1/16 (the fast Walsh-Hadamard transform in fp32); then
+ * amax = max |y|, scales[r] = amax / 448 and codes = e4m3(y * (448 / amax)),
+ * rounded to nearest even and saturated (an all-zero row: scale 0, codes 0).
+ * Used offline on the weights and, inside the block, on the activations.
+ * x: device bf16 [rows, K] (row stride ldx elements); K a multiple of 256,
+ * at most 16384.  codes: device bytes [rows, K] (row stride ldq bytes, a
+ * multiple of 16); scales: device fp32 [rows]. */
+dit_status dit_rotate_quantize(const void* x, int64_t ldx, int32_t rows, int32_t K,
+                               void* codes, int64_t ldq, float* scales, void* stream);
+
+/* dit_ln_modulate's row (same modes) rotated and coded as dit_rotate_quantize
+ * does, without writing it in bf16: the A operand of the QKV and gate/up
+ * projections in the W8A8 format.  H a multiple of 256, at most 8192.
+ * codes: device bytes [rows, H] (row stride ldq); scales: device fp32 [rows]. */
+dit_status dit_ln_modulate_rotate_quantize(int32_t mode, const float* x, int64_t ldx,
+                                           int32_t rows, int32_t H, const float* p0,
+                                           const float* p1, float eps, void* codes,
+                                           int64_t ldq, float* scales, void* stream);
+
+/* dit_linear on e4m3 codes: y[i, n] = a_scales[i] w_scales[n] sum_k a[i, k]
+ * w[n, k], accumulated in fp32 on the tensor cores, then the same epilogues
+ * as dit_linear.  a: device e4m3 [M, K] (row stride lda bytes), a_scales
+ * [M]; w: device e4m3 [N, K] (ldw bytes; [2F, K] for the GLU epilogues),
+ * w_scales [N] ([2F]).  K a multiple of 16. */
+dit_status dit_linear_e4m3(int32_t epilogue, const void* a, const float* a_scales,
+                           int64_t lda, const void* w, const float* w_scales, int64_t ldw,
+                           int32_t M, int32_t N, int32_t K, void* out, int64_t ldo,
+                           const float* bias_or_gate, void* stream);
 
 /* Timestep conditioning of one step ([ZFLOW] section IV: flip_sin_to_cos
  * sinusoid; [ERNIE] section IV, adaLN split and section V, Bug 4, final

@@ -46,7 +46,7 @@ def oracle_block_config(wl):
     return O.BlockConfig(wl.hidden, wl.n_heads, wl.n_kv_heads, wl.head_dim, wl.ffn,
                          rope_layout=wl.rope_layout, adaln=wl.adaln, qk_norm=wl.qk_norm,
                          norm_kind=wl.norm_kind, glu=wl.glu, rope_order=wl.rope_order,
-                         gate_fn=wl.gate_fn)
+                         gate_fn=wl.gate_fn, linear_format=wl.linear_format)
 
 
 def oracle_weights(w: dict) -> dict:
@@ -66,16 +66,20 @@ def _bf16(x):
 
 def bf16_storage_rows(cfg, w, x, mod, angles, rows):
     """The block on sampled rows, evaluated with oracle functions in fp32 but
-    with the intermediates the CUDA path stores in bf16 (the GEMM inputs a,
-    q/k/v, o, a2, h) rounded to bf16.  Used only to size a tolerance: it
-    measures how far bf16 storage alone moves the fp32 result."""
+    with the intermediates the CUDA path stores in bf16 rounded to bf16: the
+    GEMM inputs a and a2 (bf16 format only: the W8A8 format codes them from
+    fp32), q/k/v, o and h.  Used only to size a tolerance: it measures how far
+    bf16 storage alone moves the fp32 result (in the W8A8 format mostly
+    through the e4m3 codes that it flips)."""
     shift1, scale1, gate1, shift2, scale2, gate2 = (mod[i] for i in range(6))
-    a = _bf16(O.modulate(O.layer_norm(x, cfg.ln_eps), shift1, scale1))
+    gate1, gate2 = O.gate_act(gate1, cfg.gate_fn), O.gate_act(gate2, cfg.gate_fn)
+    keep_a = cfg.linear_format == "w8a8_h256"
+    rnd_a = (lambda t: t) if keep_a else _bf16
+    a = rnd_a(O.modulate(O.norm(x, cfg.ln_eps, cfg.norm_kind), shift1, scale1))
     q, k, v = O.qkv_heads(cfg, a, w, angles)
     q, k, v = _bf16(q), _bf16(k), _bf16(v)
     o = _bf16(O.attention_rows(q[rows], k, v, cfg.n_heads, cfg.n_kv_heads))
-    xr = O.gated_residual(x[rows], gate1, O.linear(o, w["w_o"]))
-    a2 = _bf16(O.modulate(O.layer_norm(xr, cfg.ln_eps), shift2, scale2))
-    gu = O.linear(a2, w["w_gu"])
-    h = _bf16(O.silu(gu[:, :cfg.ffn]) * gu[:, cfg.ffn:])
-    return O.gated_residual(xr, gate2, O.linear(h, w["w_down"]))
+    xr = O.gated_residual(x[rows], gate1, O.project(cfg, o, w["w_o"]))
+    a2 = rnd_a(O.modulate(O.norm(xr, cfg.ln_eps, cfg.norm_kind), shift2, scale2))
+    h = _bf16(O.glu(cfg, O.project(cfg, a2, w["w_gu"])))
+    return O.gated_residual(xr, gate2, O.project(cfg, h, w["w_down"]))

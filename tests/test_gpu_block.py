@@ -48,7 +48,7 @@ def rope_tables(wl):
 def run_block_gpu(wl, w, x, mod):
     """mod: device tensor [6, H], a CPU tensor, or None (pre-norm ViT)."""
     cfg = dit.block_config_from(wl)
-    blk = dit.DeviceBlock(w, dev())
+    blk = dit.DeviceBlock(w, dev(), wl.linear_format)
     rc, rs = rope_tables(wl)
     xg = x.to(dev()).contiguous()
     dit.dit_block_forward(cfg, blk, xg, None if mod is None else mod.to(dev()).contiguous(), rc,
@@ -278,7 +278,7 @@ def run_denoise(wl, n_layers, sigma, sigma_next):
     latent = synth.latent_input(wl, seed=1)
     text = synth.text_input(wl, seed=1)
     cfg = dit.model_config_from(wl, n_layers)
-    model = dit.DeviceModel(mw, dev())
+    model = dit.DeviceModel(mw, dev(), linear_format=wl.linear_format)
     lat = latent.to(dev()).contiguous()
     v = torch.empty_like(lat)
     dit.dit_denoise_step(cfg, model, lat, text.to(dev()) if wl.n_txt else None, wl.grid_h,
