@@ -64,7 +64,7 @@ void count_launch(int n) { t_launches += n; }
 bool make_tmap(CUtensorMap* map, uint32_t elem_bytes, const void* base, int rank,
                const uint64_t* dims, const uint64_t* strides_bytes, const uint32_t* box) {
   if (g_encode == nullptr || !aligned16(base)) return false;
-  if (elem_bytes != 1 && elem_bytes != 2) return false;
+  if (elem_bytes != 1 && elem_bytes != 2 && elem_bytes != 4) return false;
   cuuint64_t gd[5];
   cuuint64_t gs[4];
   cuuint32_t bx[5];
@@ -79,8 +79,9 @@ bool make_tmap(CUtensorMap* map, uint32_t elem_bytes, const void* base, int rank
     }
   }
   CUresult r = g_encode(map,
-                        elem_bytes == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
-                                        : CU_TENSOR_MAP_DATA_TYPE_UINT8,
+                        elem_bytes == 2   ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                        : elem_bytes == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                          : CU_TENSOR_MAP_DATA_TYPE_UINT8,
                         (cuuint32_t)rank,
                         const_cast<void*>(base), gd, gs, bx, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,

@@ -52,7 +52,57 @@ struct GemmBars {
   uint32_t tmem_slot;
 };
 
-constexpr size_t SMEM_BYTES = (size_t)STAGES * STAGE_BYTES + 1024 + sizeof(GemmBars) + 64;
+// Epilogue staging: each epilogue warp owns two buffers of 32 rows x 128
+// bytes (its TMEM lane quarter x one chunk of columns) in the 128-byte
+// swizzled layout, written by the threads and stored to global memory by TMA.
+constexpr int EBUF_BYTES = 32 * 128;
+constexpr int EPI_SMEM = 4 * 2 * EBUF_BYTES;
+
+// Epilogues that stage their output (the others keep that shared memory as L1
+// for their table and parameter loads).
+template <int EPI>
+constexpr bool is_staged() {
+  return EPI == EPI_BF16 || EPI == EPI_SWIGLU || EPI == EPI_GEGLU || EPI == EPI_RESIDUAL ||
+         EPI == EPI_RESIDUAL_TANH || EPI == EPI_RESIDUAL_SIGMOID;
+}
+template <int EPI>
+constexpr size_t smem_bytes() {
+  return (size_t)STAGES * STAGE_BYTES + (is_staged<EPI>() ? EPI_SMEM : 0) + 1024 +
+         sizeof(GemmBars) + 64;
+}
+static_assert(smem_bytes<EPI_RESIDUAL>() <= 232448, "shared memory per CTA exceeded");
+
+// One epilogue warp's staging buffers and which one is next.
+struct EpiStage {
+  uint8_t* buf;
+  int cur;
+};
+
+// Next staging buffer of this warp, once the TMA operation that read it two
+// chunks ago has finished reading.
+__device__ __forceinline__ uint8_t* ebuf_acquire(EpiStage& es, int lane) {
+  if (lane == 0) bulk_wait_read<1>();
+  __syncwarp();
+  return es.buf + es.cur * EBUF_BYTES;
+}
+
+// Makes the warp's stores to the buffer visible to the TMA unit; lane 0 then
+// issues the store and commits it.
+__device__ __forceinline__ void ebuf_release(EpiStage& es) {
+  fence_proxy_async_smem();
+  __syncwarp();
+  es.cur ^= 1;
+}
+
+// 16 bytes into row r, piece j (0..7) of a swizzled staging buffer.
+__device__ __forceinline__ void ebuf_put16(uint8_t* b, int r, int j, uint4 v) {
+  *reinterpret_cast<uint4*>(b + r * 128 + ((j ^ (r & 7)) << 4)) = v;
+}
+
+__device__ __forceinline__ uint4 pack_bf16x8(const float* v) {
+  return make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]), pack_bf16x2(v[4], v[5]),
+                    pack_bf16x2(v[6], v[7]));
+}
 
 __device__ __forceinline__ void store_bf16x32(__nv_bfloat16* dst, const float (&v)[32]) {
   uint4* d = reinterpret_cast<uint4*>(dst);
@@ -67,7 +117,9 @@ __device__ __forceinline__ void store_bf16x32(__nv_bfloat16* dst, const float (&
   }
 }
 
-__device__ __forceinline__ float silu_f(float x) { return x / (1.0f + expf(-x)); }
+// SiLU with the hardware exponential and a fast divide: relative error a few
+// fp32 ulps, far below the bf16 output's resolution.
+__device__ __forceinline__ float silu_f(float x) { return __fdividef(x, 1.0f + __expf(-x)); }
 
 // GELU by its tanh approximation, the argument limited to [-20, 20] and the
 // result to [-65504, 65504] ([ERNIE] section V, Bug 1).
@@ -141,13 +193,80 @@ __device__ __forceinline__ void scale_cols(float (&v)[32], float rs, const float
 }
 
 // ---------------------------------------------------------------- epilogues
+// row: this thread's output row; row0: the first row of its warp's slab.
 template <int EPI, int HD, bool F8>
-__device__ __forceinline__ void epilogue_tile(const GemmParams& p, uint32_t tbase, int row,
-                                              int n_blk) {
+__device__ __forceinline__ void epilogue_tile(const GemmParams& p, const CUtensorMap* tmO,
+                                              EpiStage& es, uint32_t tbase, int row, int row0,
+                                              int lane, int n_blk) {
   const bool row_ok = row < p.M;
   float rs = 1.0f;
   if constexpr (F8) rs = row_ok ? __ldg(p.sa + row) : 0.0f;
-  if constexpr (EPI == EPI_BF16 || EPI == EPI_F32_BIAS || is_residual<EPI>()) {
+  if constexpr (is_residual<EPI>()) {
+    // x += g y through the staging buffer and a TMA reduce-add: the add
+    // happens in L2, the GEMM never reads x
+#pragma unroll 1
+    for (int c = 0; c < BN / 32; ++c) {
+      const int col = n_blk * BN + c * 32;
+      if (col >= p.N) break;
+      float v[32];
+      __syncwarp();
+      tmem_ld32(tbase + c * 32, v);
+      if constexpr (F8) scale_cols(v, rs, p.sb, col, p.N);
+      if (p.vec) {
+        if (col + 32 <= p.N) {
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            const float4 g = __ldg(reinterpret_cast<const float4*>(p.vec + col) + q);
+            v[4 * q + 0] *= gate_f<EPI>(g.x);
+            v[4 * q + 1] *= gate_f<EPI>(g.y);
+            v[4 * q + 2] *= gate_f<EPI>(g.z);
+            v[4 * q + 3] *= gate_f<EPI>(g.w);
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            if (col + i < p.N) v[i] *= gate_f<EPI>(__ldg(p.vec + col + i));
+        }
+      }
+      uint8_t* b = ebuf_acquire(es, lane);
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        ebuf_put16(b, lane, q,
+                   make_uint4(__float_as_uint(v[4 * q]), __float_as_uint(v[4 * q + 1]),
+                              __float_as_uint(v[4 * q + 2]), __float_as_uint(v[4 * q + 3])));
+      ebuf_release(es);
+      if (lane == 0 && row0 < p.M) {  // a slab wholly below M stores nothing
+        tma_reduce_add_2d(tmO, b, col, row0);
+        bulk_commit();
+      }
+    }
+  } else if constexpr (EPI == EPI_BF16) {
+    // 64 columns (128 bytes of bf16) per staged chunk
+#pragma unroll 1
+    for (int c = 0; c < BN / 64; ++c) {
+      const int col = n_blk * BN + c * 64;
+      if (col >= p.N) break;
+      float v[32], w[32];
+      __syncwarp();
+      tmem_ld32(tbase + c * 64, v);
+      tmem_ld32(tbase + c * 64 + 32, w);
+      if constexpr (F8) {
+        scale_cols(v, rs, p.sb, col, p.N);
+        scale_cols(w, rs, p.sb, col + 32, p.N);
+      }
+      uint8_t* b = ebuf_acquire(es, lane);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        ebuf_put16(b, lane, q, pack_bf16x8(v + 8 * q));
+        ebuf_put16(b, lane, 4 + q, pack_bf16x8(w + 8 * q));
+      }
+      ebuf_release(es);
+      if (lane == 0 && row0 < p.M) {  // a slab wholly below M stores nothing
+        tma_store_2d(tmO, b, col, row0);
+        bulk_commit();
+      }
+    }
+  } else if constexpr (EPI == EPI_F32_BIAS) {
 #pragma unroll 1
     for (int c = 0; c < BN / 32; ++c) {
       const int col = n_blk * BN + c * 32;
@@ -158,82 +277,59 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, uint32_t tbas
       if (!row_ok) continue;  // the loads above stay warp-uniform
       if constexpr (F8) scale_cols(v, rs, p.sb, col, p.N);
       const bool full = col + 32 <= p.N;
-      if constexpr (EPI == EPI_BF16) {
-        __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(p.out) + (size_t)row * p.ldo + col;
-        if (full) {
-          store_bf16x32(dst, v);
-        } else {
-          for (int i = 0; i < 32 && col + i < p.N; ++i) dst[i] = __float2bfloat16_rn(v[i]);
-        }
-      } else if constexpr (EPI == EPI_F32_BIAS) {
-        float* dst = reinterpret_cast<float*>(p.out) + (size_t)row * p.ldo + col;
-        if (full) {
+      float* dst = reinterpret_cast<float*>(p.out) + (size_t)row * p.ldo + col;
+      if (full) {
 #pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            float4 o;
-            o.x = v[4 * q + 0];
-            o.y = v[4 * q + 1];
-            o.z = v[4 * q + 2];
-            o.w = v[4 * q + 3];
-            if (p.vec) {
-              const float4 b = __ldg(reinterpret_cast<const float4*>(p.vec + col) + q);
-              o.x += b.x; o.y += b.y; o.z += b.z; o.w += b.w;
-            }
-            reinterpret_cast<float4*>(dst)[q] = o;
+        for (int q = 0; q < 8; ++q) {
+          float4 o;
+          o.x = v[4 * q + 0];
+          o.y = v[4 * q + 1];
+          o.z = v[4 * q + 2];
+          o.w = v[4 * q + 3];
+          if (p.vec) {
+            const float4 b = __ldg(reinterpret_cast<const float4*>(p.vec + col) + q);
+            o.x += b.x; o.y += b.y; o.z += b.z; o.w += b.w;
           }
-        } else {
-          for (int i = 0; i < 32 && col + i < p.N; ++i)
-            dst[i] = v[i] + (p.vec ? __ldg(p.vec + col + i) : 0.0f);
+          reinterpret_cast<float4*>(dst)[q] = o;
         }
-      } else {  // gated residual
-        float* dst = reinterpret_cast<float*>(p.out) + (size_t)row * p.ldo + col;
-        if (full) {
-#pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            float4 x = reinterpret_cast<float4*>(dst)[q];
-            float4 g = make_float4(1.f, 1.f, 1.f, 1.f);
-            if (p.vec) {
-              g = __ldg(reinterpret_cast<const float4*>(p.vec + col) + q);
-              g.x = gate_f<EPI>(g.x);
-              g.y = gate_f<EPI>(g.y);
-              g.z = gate_f<EPI>(g.z);
-              g.w = gate_f<EPI>(g.w);
-            }
-            x.x = fmaf(g.x, v[4 * q + 0], x.x);
-            x.y = fmaf(g.y, v[4 * q + 1], x.y);
-            x.z = fmaf(g.z, v[4 * q + 2], x.z);
-            x.w = fmaf(g.w, v[4 * q + 3], x.w);
-            reinterpret_cast<float4*>(dst)[q] = x;
-          }
-        } else {
-          for (int i = 0; i < 32 && col + i < p.N; ++i)
-            dst[i] = fmaf(p.vec ? gate_f<EPI>(__ldg(p.vec + col + i)) : 1.0f, v[i], dst[i]);
-        }
+      } else {
+        for (int i = 0; i < 32 && col + i < p.N; ++i)
+          dst[i] = v[i] + (p.vec ? __ldg(p.vec + col + i) : 0.0f);
       }
     }
   } else if constexpr (EPI == EPI_SWIGLU || EPI == EPI_GEGLU) {
-    // Accumulator columns [0, 128) are gate rows, [128, 256) the matching up rows.
+    // Accumulator columns [0, 128) are gate rows, [128, 256) the matching up
+    // rows; h leaves in two staged chunks of 64 columns.
 #pragma unroll 1
-    for (int c = 0; c < 4; ++c) {
-      float g[32], u[32];
-      __syncwarp();
-      tmem_ld32(tbase + c * 32, g);
-      tmem_ld32(tbase + 128 + c * 32, u);
-      if (!row_ok) continue;
-      if constexpr (F8) {  // gate rows' scales first, then the up rows'
-        scale_cols(g, rs, p.sb, n_blk * 128 + c * 32, p.N);
-        scale_cols(u, rs, p.sb + p.N, n_blk * 128 + c * 32, p.N);
-      }
-      if constexpr (EPI == EPI_GEGLU) {
+    for (int c2 = 0; c2 < 2; ++c2) {
+      uint8_t* b = nullptr;
+#pragma unroll 1
+      for (int half = 0; half < 2; ++half) {
+        const int cc = c2 * 64 + half * 32;
+        float g[32], u[32];
+        __syncwarp();
+        tmem_ld32(tbase + cc, g);
+        tmem_ld32(tbase + 128 + cc, u);
+        if constexpr (F8) {  // gate rows' scales first, then the up rows'
+          scale_cols(g, rs, p.sb, n_blk * 128 + cc, p.N);
+          scale_cols(u, rs, p.sb + p.N, n_blk * 128 + cc, p.N);
+        }
+        if constexpr (EPI == EPI_GEGLU) {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) g[i] = gelu_tanh_clamped_f(g[i]) * u[i];
-      } else {
+          for (int i = 0; i < 32; ++i) g[i] = gelu_tanh_clamped_f(g[i]) * u[i];
+        } else {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) g[i] = silu_f(g[i]) * u[i];
+          for (int i = 0; i < 32; ++i) g[i] = silu_f(g[i]) * u[i];
+        }
+        if (half == 0) b = ebuf_acquire(es, lane);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) ebuf_put16(b, lane, half * 4 + q, pack_bf16x8(g + 8 * q));
       }
-      __nv_bfloat16* dst =
-          reinterpret_cast<__nv_bfloat16*>(p.out) + (size_t)row * p.ldo + n_blk * 128 + c * 32;
-      store_bf16x32(dst, g);
+      ebuf_release(es);
+      if (lane == 0 && row0 < p.M) {  // a slab wholly below M stores nothing
+        tma_store_2d(tmO, b, n_blk * 128 + c2 * 64, row0);
+        bulk_commit();
+      }
     }
   } else if constexpr (EPI == EPI_QKV) {
     const QkvEpi& q = p.qkv;
@@ -301,11 +397,12 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, uint32_t tbas
 template <int EPI, int HD, bool F8>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                const GemmParams p) {
+                const __grid_constant__ CUtensorMap tmO, const GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  GemmBars* bars = reinterpret_cast<GemmBars*>(smem + (size_t)STAGES * STAGE_BYTES);
+  GemmBars* bars = reinterpret_cast<GemmBars*>(smem + (size_t)STAGES * STAGE_BYTES +
+                                               (is_staged<EPI>() ? EPI_SMEM : 0));
 
   const int warp = warp_id(), lane = lane_id();
   const int num_tiles = p.num_m * p.num_n;
@@ -418,6 +515,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // -------------------------------------------------- epilogue warps
     const int quarter = warp & 3;  // TMEM lanes [32 quarter, 32 quarter + 32)
     const int r_in = quarter * 32 + lane;
+    EpiStage es{smem + (size_t)STAGES * STAGE_BYTES + (size_t)quarter * 2 * EBUF_BYTES, 0};
     int local = 0;
     for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++local) {
       const int m_blk = t % p.num_m, n_blk = t / p.num_m;
@@ -426,11 +524,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       if (!mbar_wait(&bars->tfull[acc], acc_phase, p.err)) break;
       tc_fence_after();
       const uint32_t tbase = tmem_base + (uint32_t)(acc * BN) + ((uint32_t)(quarter * 32) << 16);
-      epilogue_tile<EPI, HD, F8>(p, tbase, m_blk * BM + r_in, n_blk);
+      epilogue_tile<EPI, HD, F8>(p, &tmO, es, tbase, m_blk * BM + r_in, m_blk * BM + quarter * 32,
+                                 lane, n_blk);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars->tempty[acc]);
     }
+    if (lane == 0) bulk_wait<0>();  // every staged store has completed
   }
 
   tc_fence_before();
@@ -442,19 +542,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 }
 
 template <int EPI, int HD, bool F8>
-cudaError_t launch_impl(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p,
-                        int grid, cudaStream_t st) {
+cudaError_t launch_impl(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& to,
+                        const GemmParams& p, int grid, cudaStream_t st) {
   static bool attr_set[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 64 && !attr_set[dev]) {
     cudaError_t e = cudaFuncSetAttribute(gemm_kernel<EPI, HD, F8>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)SMEM_BYTES);
+                                         (int)smem_bytes<EPI>());
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
-  gemm_kernel<EPI, HD, F8><<<grid, NUM_THREADS, SMEM_BYTES, st>>>(ta, tb, p);
+  gemm_kernel<EPI, HD, F8><<<grid, NUM_THREADS, smem_bytes<EPI>(), st>>>(ta, tb, to, p);
   count_launch();
   return cudaGetLastError();
 }
@@ -483,23 +583,34 @@ cudaError_t launch_gemm_t(int epi, int hd, const void* A, long long lda, const v
     const uint32_t box[2] = {BK, glu ? 128u : (uint32_t)BN};
     if (!make_tmap(&tb, ES, B, 2, dims, strides, box)) return cudaErrorInvalidValue;
   }
+  // the output map of the staged epilogues (unused by the others): fp32
+  // boxes of 32 x 32 for the residual reduce-add, bf16 boxes of 64 x 32
+  CUtensorMap to = ta;
+  const bool resid = epi == EPI_RESIDUAL || epi == EPI_RESIDUAL_TANH || epi == EPI_RESIDUAL_SIGMOID;
+  if (resid || glu || epi == EPI_BF16) {
+    const uint32_t oes = resid ? 4 : 2;
+    const uint64_t dims[2] = {(uint64_t)p.N, (uint64_t)p.M};
+    const uint64_t strides[1] = {(uint64_t)p.ldo * oes};
+    const uint32_t box[2] = {resid ? 32u : 64u, 32u};
+    if (!make_tmap(&to, oes, p.out, 2, dims, strides, box)) return cudaErrorInvalidValue;
+  }
   p.num_m = (p.M + BM - 1) / BM;
   p.num_n = glu ? p.N / 128 : (p.N + BN - 1) / BN;
   p.err = dev_err(ds);
   const int tiles = p.num_m * p.num_n;
   const int grid = tiles < ds->sm_count ? tiles : ds->sm_count;
   switch (epi) {
-    case EPI_BF16: return launch_impl<EPI_BF16, 0, F8>(ta, tb, p, grid, st);
-    case EPI_F32_BIAS: return launch_impl<EPI_F32_BIAS, 0, F8>(ta, tb, p, grid, st);
-    case EPI_RESIDUAL: return launch_impl<EPI_RESIDUAL, 0, F8>(ta, tb, p, grid, st);
-    case EPI_SWIGLU: return launch_impl<EPI_SWIGLU, 0, F8>(ta, tb, p, grid, st);
-    case EPI_GEGLU: return launch_impl<EPI_GEGLU, 0, F8>(ta, tb, p, grid, st);
-    case EPI_RESIDUAL_TANH: return launch_impl<EPI_RESIDUAL_TANH, 0, F8>(ta, tb, p, grid, st);
+    case EPI_BF16: return launch_impl<EPI_BF16, 0, F8>(ta, tb, to, p, grid, st);
+    case EPI_F32_BIAS: return launch_impl<EPI_F32_BIAS, 0, F8>(ta, tb, to, p, grid, st);
+    case EPI_RESIDUAL: return launch_impl<EPI_RESIDUAL, 0, F8>(ta, tb, to, p, grid, st);
+    case EPI_SWIGLU: return launch_impl<EPI_SWIGLU, 0, F8>(ta, tb, to, p, grid, st);
+    case EPI_GEGLU: return launch_impl<EPI_GEGLU, 0, F8>(ta, tb, to, p, grid, st);
+    case EPI_RESIDUAL_TANH: return launch_impl<EPI_RESIDUAL_TANH, 0, F8>(ta, tb, to, p, grid, st);
     case EPI_RESIDUAL_SIGMOID:
-      return launch_impl<EPI_RESIDUAL_SIGMOID, 0, F8>(ta, tb, p, grid, st);
+      return launch_impl<EPI_RESIDUAL_SIGMOID, 0, F8>(ta, tb, to, p, grid, st);
     case EPI_QKV:
-      if (hd == 64) return launch_impl<EPI_QKV, 64, F8>(ta, tb, p, grid, st);
-      if (hd == 128) return launch_impl<EPI_QKV, 128, F8>(ta, tb, p, grid, st);
+      if (hd == 64) return launch_impl<EPI_QKV, 64, F8>(ta, tb, to, p, grid, st);
+      if (hd == 128) return launch_impl<EPI_QKV, 128, F8>(ta, tb, to, p, grid, st);
       return cudaErrorInvalidValue;
     default: return cudaErrorInvalidValue;
   }

@@ -7,19 +7,24 @@
 // Hadamard matrix scaled by 1/16, then coded in e4m3 with one fp32 scale:
 // amax = max |y|, scale = amax / 448, code = e4m3(y * (448 / amax)) rounded
 // to nearest even and saturated.  The rotation is the fast Walsh-Hadamard
-// transform: butterfly spans 1, 2 and 4 inside a thread's 8 consecutive
-// values, spans 8 ... 128 between the 32 lanes of a warp, so one warp owns one
-// 256-wide block and no shared memory is touched until the row maximum.
+// transform with the butterfly spans in the order 1, 2, ..., 128, every
+// butterfly one fp32 add or subtract, so the result does not depend on how
+// the spans are spread over threads.
 //
-//   rotq_kernel     bf16 rows (weights offline; attention output and GLU
-//                   output online) -> codes + scales
-//   ln_rotq_kernel  the fp32 residual rows through LayerNorm/RMSNorm and the
-//                   AdaLN or affine modulation, then rotated and coded: the
-//                   A operand of the QKV and gate/up projections written
-//                   once, in 8 bits
-//
-// One 256-thread block per row; the row stays in registers (K <= 256 * 8 *
-// MAXC).  Loads and stores are 16- and 8-byte vectors, coalesced per warp.
+//   rotq_tma_kernel     bf16 rows (weights offline; attention output and GLU
+//                       output online) -> codes + scales
+//   ln_rotq_tma_kernel  the fp32 residual rows through LayerNorm/RMSNorm and
+//                       the AdaLN or affine modulation, then rotated and
+//                       coded: the A operand of the QKV and gate/up
+//                       projections written once, in 8 bits
+// Both are persistent: a ring of whole rows in shared memory filled by one
+// TMA copy per row (128-byte swizzle, so that the reads below are free of
+// bank conflicts), one row per pass of the CTA, K / 32 threads, each owning
+// 32 consecutive values: spans 1..16 inside the thread (packed fp32 pairs
+// from span 2), spans 32, 64, 128 between the 8 threads of a 256-block.
+// One barrier per row for the bf16 rows (three for the normed rows: mean,
+// variance, maximum).  Rows whose K is not a multiple of 1024 (or too long)
+// take the warp-per-block kernels rotq_kernel / ln_rotq_kernel instead.
 #include "internal.h"
 
 namespace dit {
@@ -199,6 +204,316 @@ __global__ void __launch_bounds__(RQ_THREADS) ln_rotq_kernel(
   code_row<MAXC>(v, nchunks, row, q, ldq, scale, red);
 }
 
+// ------------------------------------------------------------ TMA-ring kernels
+constexpr int RQT_STAGES = 4;
+constexpr int RQT_MAX_THREADS = 512;     // K <= 16384
+constexpr int RQT_LN_MAX_THREADS = 256;  // H <= 8192
+
+__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
+  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) &
+                                    ~static_cast<uintptr_t>(1023));
+}
+
+// x H over this thread's 32 values (elements 32 j + e of a 256-block, j =
+// lane % 8), spans 1, 2, ..., 128 in order; then the exact scaling by 1/16.
+__device__ __forceinline__ void fwht256_seg32(float (&v)[32], int lane) {
+#pragma unroll
+  for (int i = 0; i < 32; i += 2) {  // span 1
+    const float a = v[i], b = v[i + 1];
+    v[i] = a + b;
+    v[i + 1] = a - b;
+  }
+  const float2 neg1 = make_float2(-1.0f, -1.0f);
+#pragma unroll
+  for (int h = 1; h < 16; h <<= 1) {  // spans 2, 4, 8, 16 on pairs (2j, 2j+1)
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      if (!(j & h)) {
+        const float2 a = make_float2(v[2 * j], v[2 * j + 1]);
+        const float2 b = make_float2(v[2 * (j + h)], v[2 * (j + h) + 1]);
+        const float2 s = __fadd2_rn(a, b);
+        const float2 d = __ffma2_rn(b, neg1, a);  // a - b, one rounding
+        v[2 * j] = s.x;
+        v[2 * j + 1] = s.y;
+        v[2 * (j + h)] = d.x;
+        v[2 * (j + h) + 1] = d.y;
+      }
+    }
+  }
+#pragma unroll
+  for (int m = 1; m < 8; m <<= 1) {  // spans 32, 64, 128 between lanes
+    const float sg = (lane & m) ? -1.0f : 1.0f;  // upper index: partner - mine
+    const float2 sg2 = make_float2(sg, sg);
+#pragma unroll
+    for (int i = 0; i < 32; i += 2) {
+      const float2 o = make_float2(__shfl_xor_sync(0xffffffffu, v[i], m),
+                                   __shfl_xor_sync(0xffffffffu, v[i + 1], m));
+      const float2 r = __ffma2_rn(sg2, make_float2(v[i], v[i + 1]), o);
+      v[i] = r.x;
+      v[i + 1] = r.y;
+    }
+  }
+  const float2 sixteenth = make_float2(0.0625f, 0.0625f);
+#pragma unroll
+  for (int i = 0; i < 32; i += 2) {
+    const float2 r = __fmul2_rn(make_float2(v[i], v[i + 1]), sixteenth);
+    v[i] = r.x;
+    v[i + 1] = r.y;
+  }
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// Codes this thread's 32 rotated values with the row's maximum and stores
+// them (32 bytes) at dst; thread 0 stores the scale.
+__device__ __forceinline__ void code_seg32(const float (&v)[32], float amax, uint8_t* dst,
+                                           float* scale_out) {
+  const float inv = amax > 0.0f ? __fdiv_rn(448.0f, amax) : 0.0f;
+  if (threadIdx.x == 0) *scale_out = amax > 0.0f ? __fdiv_rn(amax, 448.0f) : 0.0f;
+  const float2 inv2 = make_float2(inv, inv);
+  uint32_t w[8];
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    const float2 a = __fmul2_rn(make_float2(v[4 * q], v[4 * q + 1]), inv2);
+    const float2 b = __fmul2_rn(make_float2(v[4 * q + 2], v[4 * q + 3]), inv2);
+    w[q] = pack_e4m3x4(a.x, a.y, b.x, b.y);
+  }
+  uint4* d = reinterpret_cast<uint4*>(dst);
+  d[0] = make_uint4(w[0], w[1], w[2], w[3]);
+  d[1] = make_uint4(w[4], w[5], w[6], w[7]);
+}
+
+// Issues the TMA copy of row `row` into ring stage `s` (one elected thread).
+__device__ __forceinline__ void rqt_issue(uint8_t* smem, int row_bytes, uint64_t* full, int s,
+                                          const CUtensorMap* tm, int row) {
+  mbar_arrive_expect_tx(&full[s], (uint32_t)row_bytes);
+  tma_load_3d(smem + (size_t)s * row_bytes, tm, &full[s], 0, 0, row);
+}
+
+// After a wait that ran out: every copy still in flight must land before the
+// CTA may exit.  Rows n in [first, issued) of this CTA went to stage n % S.
+__device__ __forceinline__ void rqt_drain(uint64_t* full, int first, int issued, const DevErr& e) {
+  for (int n = first; n < issued; ++n)
+    mbar_wait(&full[n % RQT_STAGES], (uint32_t)((n / RQT_STAGES) & 1), e);
+}
+
+// bf16 rows [rows, K] (3-D map: 64 x K/64 x rows, box one row) -> codes.
+__global__ void __launch_bounds__(RQT_MAX_THREADS) rotq_tma_kernel(
+    const __grid_constant__ CUtensorMap tm, int rows, int K, uint8_t* __restrict__ q,
+    long long ldq, float* __restrict__ scale, DevErr err) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  const int row_bytes = K * 2;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)RQT_STAGES * row_bytes);
+  __shared__ float red[2][RQT_MAX_THREADS / 32];
+  const int t = threadIdx.x, warp = t >> 5, lane = t & 31, nwarps = blockDim.x >> 5;
+  const int G = gridDim.x;
+  int issued = 0;  // rows of this CTA whose copy has been issued (thread 0)
+  if (t == 0) {
+    for (int s = 0; s < RQT_STAGES; ++s) mbar_init(&full[s], 1);
+    fence_barrier_init();
+    tma_prefetch_desc(&tm);
+    for (int s = 0; s < RQT_STAGES && blockIdx.x + s * G < rows; ++s, ++issued)
+      rqt_issue(smem, row_bytes, full, s, &tm, blockIdx.x + s * G);
+  }
+  __syncthreads();
+  // this thread's 64 bytes: half (t & 1) of 128-byte line t >> 1
+  const int L = t >> 1, half = t & 1;
+  int it = 0;
+  for (int row = blockIdx.x; row < rows; row += G, ++it) {
+    const int s = it % RQT_STAGES;
+    const bool ok = mbar_wait(&full[s], (uint32_t)((it / RQT_STAGES) & 1), err);
+    float v[32];
+    const uint8_t* line = smem + (size_t)s * row_bytes + (size_t)L * 128;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const uint4 u = *reinterpret_cast<const uint4*>(line + (((half * 4 + k) ^ (L & 7)) << 4));
+      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        v[8 * k + 2 * i] = __uint_as_float(w[i] << 16);
+        v[8 * k + 2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+      }
+    }
+    fwht256_seg32(v, lane);
+    float m = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) m = fmaxf(m, fabsf(v[i]));
+    m = warp_max(m);
+    if (lane == 0) red[it & 1][warp] = m;
+    // every thread has read stage s and published its maximum
+    if (!__syncthreads_and(ok)) {
+      if (t == 0) rqt_drain(full, it, issued, err);
+      break;
+    }
+    if (t == 0 && row + RQT_STAGES * G < rows) {
+      rqt_issue(smem, row_bytes, full, s, &tm, row + RQT_STAGES * G);
+      ++issued;
+    }
+    float amax = red[it & 1][0];
+    for (int w2 = 1; w2 < nwarps; ++w2) amax = fmaxf(amax, red[it & 1][w2]);
+    code_seg32(v, amax, q + (size_t)row * ldq + (size_t)t * 32, scale + row);
+  }
+}
+
+// fp32 rows [rows, H] (3-D map: 32 x H/32 x rows) through the norm and the
+// modulation, rotated and coded.  MODE bit 0: affine n g + b (else AdaLN
+// n (1 + scale) + shift); RMS: RMSNorm.
+template <int MODE, bool RMS>
+__global__ void __launch_bounds__(RQT_LN_MAX_THREADS) ln_rotq_tma_kernel(
+    const __grid_constant__ CUtensorMap tm, int rows, int H, const float* __restrict__ p0,
+    const float* __restrict__ p1, float eps, uint8_t* __restrict__ q, long long ldq,
+    float* __restrict__ scale, DevErr err) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  const int row_bytes = H * 4;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)RQT_STAGES * row_bytes);
+  __shared__ float red_s[RQT_MAX_THREADS / 32], red_v[RQT_MAX_THREADS / 32],
+      red_m[RQT_MAX_THREADS / 32];
+  const int t = threadIdx.x, warp = t >> 5, lane = t & 31, nwarps = blockDim.x >> 5;
+  const int G = gridDim.x;
+  int issued = 0;
+  if (t == 0) {
+    for (int s = 0; s < RQT_STAGES; ++s) mbar_init(&full[s], 1);
+    fence_barrier_init();
+    tma_prefetch_desc(&tm);
+    for (int s = 0; s < RQT_STAGES && blockIdx.x + s * G < rows; ++s, ++issued)
+      rqt_issue(smem, row_bytes, full, s, &tm, blockIdx.x + s * G);
+  }
+  // this thread's modulation parameters (32 consecutive columns), kept in
+  // registers for every row
+  float pa[32], pb[32];
+  {
+    const float4* a4 = reinterpret_cast<const float4*>(p0 + (size_t)t * 32);
+    const float4* b4 = reinterpret_cast<const float4*>(p1 + (size_t)t * 32);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float4 a = __ldg(a4 + i), b = __ldg(b4 + i);
+      pa[4 * i] = a.x; pa[4 * i + 1] = a.y; pa[4 * i + 2] = a.z; pa[4 * i + 3] = a.w;
+      pb[4 * i] = b.x; pb[4 * i + 1] = b.y; pb[4 * i + 2] = b.z; pb[4 * i + 3] = b.w;
+    }
+  }
+  __syncthreads();
+  int it = 0;
+  for (int row = blockIdx.x; row < rows; row += G, ++it) {
+    const int s = it % RQT_STAGES;
+    const bool ok = mbar_wait(&full[s], (uint32_t)((it / RQT_STAGES) & 1), err);
+    float v[32];
+    const uint8_t* line = smem + (size_t)s * row_bytes + (size_t)t * 128;
+#pragma unroll
+    for (int p = 0; p < 8; ++p) {
+      const float4 f = *reinterpret_cast<const float4*>(line + ((p ^ (t & 7)) << 4));
+      v[4 * p] = f.x; v[4 * p + 1] = f.y; v[4 * p + 2] = f.z; v[4 * p + 3] = f.w;
+    }
+    float sum = 0.f;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) sum += v[i];
+    sum = warp_sum(sum);
+    if (lane == 0) red_s[warp] = sum;
+    if (!__syncthreads_and(ok)) {
+      if (t == 0) rqt_drain(full, it, issued, err);
+      break;
+    }
+    // stage s is free again
+    if (t == 0 && row + RQT_STAGES * G < rows) {
+      rqt_issue(smem, row_bytes, full, s, &tm, row + RQT_STAGES * G);
+      ++issued;
+    }
+    float mean = 0.f;
+    if (!RMS) {
+      for (int w2 = 0; w2 < nwarps; ++w2) mean += red_s[w2];
+      mean /= (float)H;
+    }
+    float ss = 0.f;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      v[i] -= mean;
+      ss = fmaf(v[i], v[i], ss);
+    }
+    ss = warp_sum(ss);
+    if (lane == 0) red_v[warp] = ss;
+    __syncthreads();
+    float var = 0.f;
+    for (int w2 = 0; w2 < nwarps; ++w2) var += red_v[w2];
+    const float rstd = 1.0f / sqrtf(var / (float)H + eps);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const float n = v[i] * rstd;
+      v[i] = (MODE & 1) ? fmaf(n, pa[i], pb[i]) : fmaf(n, 1.0f + pb[i], pa[i]);
+    }
+    fwht256_seg32(v, lane);
+    float m = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) m = fmaxf(m, fabsf(v[i]));
+    m = warp_max(m);
+    if (lane == 0) red_m[warp] = m;
+    __syncthreads();
+    float amax = red_m[0];
+    for (int w2 = 1; w2 < nwarps; ++w2) amax = fmaxf(amax, red_m[w2]);
+    code_seg32(v, amax, q + (size_t)row * ldq + (size_t)t * 32, scale + row);
+  }
+}
+
+size_t rqt_smem_bytes(int row_bytes) {
+  return (size_t)RQT_STAGES * row_bytes + 1024 + RQT_STAGES * sizeof(uint64_t) + 64;
+}
+
+// Persistent grid: as many CTAs as fit on an SM (queried once per device,
+// kernel variant and row length), times the SMs, at most one per row.
+template <typename Kern>
+cudaError_t rqt_grid(Kern kern, int variant, int threads, int row_bytes, int rows, int* grid) {
+  constexpr int MAXDEV = 64, VARIANTS = 5, LENGTHS = 33;
+  static int occ[MAXDEV][VARIANTS][LENGTHS];
+  static bool attr[MAXDEV][VARIANTS];
+  const DeviceState* ds = device_state();
+  int dev = 0;
+  if (!ds || cudaGetDevice(&dev) != cudaSuccess || dev >= MAXDEV) return cudaErrorInitializationError;
+  const int li = row_bytes / 2048;  // row_bytes is a multiple of 2048, at most 65536
+  if (variant >= VARIANTS || li >= LENGTHS) return cudaErrorInvalidValue;
+  const size_t smem = rqt_smem_bytes(row_bytes);
+  if (!attr[dev][variant]) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)rqt_smem_bytes(32768));
+    if (e != cudaSuccess) return e;
+    attr[dev][variant] = true;
+  }
+  if (occ[dev][variant][li] == 0) {
+    int per_sm = 0;
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, smem);
+    if (e != cudaSuccess) return e;
+    if (per_sm < 1) return cudaErrorInvalidConfiguration;
+    occ[dev][variant][li] = per_sm;
+  }
+  const long long cap = (long long)occ[dev][variant][li] * ds->sm_count;
+  *grid = (int)(rows < cap ? rows : cap);
+  return cudaSuccess;
+}
+
+template <int MODE, bool RMS>
+cudaError_t ln_rotq_tma_launch(const CUtensorMap& tm, int rows, int H, const float* p0,
+                               const float* p1, float eps, uint8_t* q, long long ldq,
+                               float* scale, cudaStream_t st) {
+  const int threads = H / 32, row_bytes = H * 4;
+  int grid = 0;
+  cudaError_t e = rqt_grid(ln_rotq_tma_kernel<MODE, RMS>, 1 + MODE + (RMS ? 2 : 0), threads,
+                           row_bytes, rows, &grid);
+  if (e != cudaSuccess) return e;
+  ln_rotq_tma_kernel<MODE, RMS><<<grid, threads, rqt_smem_bytes(row_bytes), st>>>(
+      tm, rows, H, p0, p1, eps, q, ldq, scale, dev_err(device_state()));
+  count_launch();
+  return cudaGetLastError();
+}
+
 bool aligned(const void* p, unsigned a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 template <int MAXC>
@@ -237,6 +552,20 @@ cudaError_t launch_rotate_quant(const __nv_bfloat16* x, long long ldx, int rows,
   if (rows < 0 || K <= 0 || K % 256 != 0 || K > ROTQ_MAX_K || ldx < K || ldq < K ||
       ldx % 8 != 0 || ldq % 16 != 0 || !aligned(x, 16) || !aligned(q, 16) || !aligned(scale, 4))
     return cudaErrorInvalidValue;
+  if (K % 1024 == 0) {  // the TMA-ring kernel: K / 32 threads, one 3-D copy per row
+    CUtensorMap tm;
+    const uint64_t dims[3] = {64, (uint64_t)K / 64, (uint64_t)rows};
+    const uint64_t strides[2] = {128, (uint64_t)ldx * 2};
+    const uint32_t box[3] = {64, (uint32_t)K / 64, 1};
+    if (!make_tmap(&tm, 2, x, 3, dims, strides, box)) return cudaErrorInvalidValue;
+    int grid = 0;
+    cudaError_t e = rqt_grid(rotq_tma_kernel, 0, K / 32, K * 2, rows, &grid);
+    if (e != cudaSuccess) return e;
+    rotq_tma_kernel<<<grid, K / 32, rqt_smem_bytes(K * 2), st>>>(tm, rows, K, q, ldq, scale,
+                                                                 dev_err(device_state()));
+    count_launch();
+    return cudaGetLastError();
+  }
   const int per_warp = (K / 256 + RQ_WARPS - 1) / RQ_WARPS;
   if (per_warp <= 1) return rotq_launch<1>(x, ldx, rows, K, q, ldq, scale, st);
   if (per_warp <= 2) return rotq_launch<2>(x, ldx, rows, K, q, ldq, scale, st);
@@ -252,6 +581,19 @@ cudaError_t launch_ln_rotate_quant(int mode, const float* x, long long ldx, int 
       ldx % 4 != 0 || ldq % 16 != 0 || !aligned(x, 16) || !aligned(p0, 16) ||
       !aligned(p1, 16) || !aligned(q, 16) || !aligned(scale, 4) || mode < 0 || mode > 3)
     return cudaErrorInvalidValue;
+  if (H % 1024 == 0) {  // the TMA-ring kernel: H / 32 threads, one 3-D copy per row
+    CUtensorMap tm;
+    const uint64_t dims[3] = {32, (uint64_t)H / 32, (uint64_t)rows};
+    const uint64_t strides[2] = {128, (uint64_t)ldx * 4};
+    const uint32_t box[3] = {32, (uint32_t)H / 32, 1};
+    if (!make_tmap(&tm, 4, x, 3, dims, strides, box)) return cudaErrorInvalidValue;
+    switch (mode) {
+      case 0: return ln_rotq_tma_launch<0, false>(tm, rows, H, p0, p1, eps, q, ldq, scale, st);
+      case 1: return ln_rotq_tma_launch<1, false>(tm, rows, H, p0, p1, eps, q, ldq, scale, st);
+      case 2: return ln_rotq_tma_launch<0, true>(tm, rows, H, p0, p1, eps, q, ldq, scale, st);
+      default: return ln_rotq_tma_launch<1, true>(tm, rows, H, p0, p1, eps, q, ldq, scale, st);
+    }
+  }
   switch (mode) {
     case 0: return ln_rotq_dispatch<0, false>(x, ldx, rows, H, p0, p1, eps, q, ldq, scale, st);
     case 1: return ln_rotq_dispatch<1, false>(x, ldx, rows, H, p0, p1, eps, q, ldq, scale, st);
