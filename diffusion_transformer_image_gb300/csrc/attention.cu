@@ -13,8 +13,8 @@
 //   warp 2       TMA producer: v tiles (transposed, 128 keys)
 //   warp 1       TMEM allocator and MMA issuer, per key block j and tile t:
 //                  O_t += P_t(j) v_j  (P read from TMEM), then
-//                  S_t(j+1) = q_t k_{j+1}^T once that PV has completed,
-//                  since P_t(j) occupies S_t's columns.
+//                  S_t(j+1) = q_t k_{j+1}^T into the columns P_t(j) occupies
+//                  (issue order is execution order on the tensor core).
 //   warps 3..18  softmax, eight per tile: query row r of tile t is shared by
 //                two warps (the same TMEM lane quarter), each owning 64 of
 //                the 128 scores of a block.  They exchange row maxima through
@@ -249,11 +249,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         umma_commit(&bars->s_full[1]);
         umma_commit(&bars->k_empty[0]);
       }
-      // Per key block j, tile by tile: O_t += P_t(j) v_j, then (once that
-      // has completed, since P_t(j) occupies S_t's columns) S_t(j+1).  Tile
-      // A's chain never waits on tile B's softmax, so the two softmax groups
-      // alternate on the special-function units while the tensor core works
-      // on the other tile.
+      // Per key block j, tile by tile: O_t += P_t(j) v_j, then S_t(j+1)
+      // (queued behind that PV).  Tile A's chain never waits on tile B's
+      // softmax, so the two softmax groups alternate on the special-function
+      // units while the tensor core works on the other tile.
       for (int j = 0; j < nb && ok; ++j) {
         const int vs = j % L::VS;
         const uint32_t v_addr = smem_u32(smem + L::OFF_V + vs * L::V_BYTES);
@@ -271,8 +270,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           umma_commit(&bars->pv_done[t]);
           if (t == 1) umma_commit(&bars->v_empty[vs]);
           if (j + 1 < nb) {
-            if ((t == 0 && !mbar_wait(&bars->k_full[st], ((j + 1) / L::KS) & 1, p.err)) ||
-                !mbar_wait(&bars->pv_done[t], j & 1, p.err)) {
+            // S_t(j+1) overwrites the columns P_t(j) occupies; the tensor core
+            // performs one thread's MMAs in issue order, so PV_t(j) has read
+            // P_t(j) before S_t(j+1) writes there and no wait is needed.
+            if (t == 0 && !mbar_wait(&bars->k_full[st], ((j + 1) / L::KS) & 1, p.err)) {
               ok = false;
               break;
             }
