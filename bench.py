@@ -501,6 +501,9 @@ def run_ours(args, rank, world, local):
     hbm_peak = peak_value(peaks, "hbm_gbs")
     kernels = {}
     ln_bytes = 6.0 * wl.n_tokens * wl.hidden
+    # ncu DRAM bytes per launch (profiles/traffic.txt), null once stale
+    traffic_keys = {"ln_modulate": "ln_modulate", "qkv": "gemm_qkv", "attention": "attention",
+                    "out": "gemm_out", "gate_up": "gemm_gate_up", "down": "gemm_down"}
     for name, ms in stages.items():
         if name == "ln_modulate":
             gbs = 2 * ln_bytes / (ms * 1e-3) / 1e9   # two launches per block in `ms`
@@ -512,9 +515,9 @@ def run_ours(args, rank, world, local):
             kernels[name] = {"ms_per_block": round(ms, 4), "bound": "tensor",
                              "achieved": round(tf, 1), "unit": "TFLOP/s",
                              "frac": round(tf / tc_peak, 3)}
+        kernels[name]["traffic"] = traffic_for(traffic_keys[name])
     dom = max((k for k in kernels if k != "ln_modulate"), key=lambda k: kernels[k]["ms_per_block"])
-    traffic_key = {"qkv": "gemm_qkv", "attention": "attention", "out": "gemm_out",
-                   "gate_up": "gemm_gate_up", "down": "gemm_down"}[dom]
+    traffic_key = traffic_keys[dom]
     roof = {"kernel": dom, "bound": "tensor", "achieved": kernels[dom]["achieved"],
             "peak": tc_peak, "unit": "TFLOP/s", "frac": kernels[dom]["frac"],
             "traffic": traffic_for(traffic_key),
@@ -610,6 +613,10 @@ def run_ours(args, rank, world, local):
         bytes_rq = {"ln_rotate_quantize": 2 * 5.0 * n_el * wl.hidden,    # two launches
                     "rotate_quantize_o": 3.0 * n_el * wl.n_heads * wl.head_dim,
                     "rotate_quantize_h": 3.0 * n_el * wl.ffn}
+        traffic8 = {"ln_rotate_quantize": "ln_rotate_quantize", "qkv": "f8_qkv",
+                    "attention": "attention", "rotate_quantize_o": "rotate_quantize_o",
+                    "out": "f8_out", "gate_up": "f8_gate_up",
+                    "rotate_quantize_h": "rotate_quantize_h", "down": "f8_down"}
         for name, ms in st8.items():
             if name in bytes_rq:
                 gbs = bytes_rq[name] / (ms * 1e-3) / 1e9
@@ -623,6 +630,7 @@ def run_ours(args, rank, world, local):
                             "achieved": round(tf, 1), "unit": "TFLOP/s",
                             "frac": round(tf / pk, 3),
                             "dtype": "bf16" if name == "attention" else "e4m3"}
+            k8[name]["traffic"] = traffic_for(traffic8[name])
         bws8 = dit.workspace(dit.dit_block_workspace_bytes(cfg8.block, wl.n_tokens), dev)
         xv = x.clone()
         ms_b8 = time_ms(lambda: dit.dit_block_forward(cfg8.block, blocks8[0], xv, mod, rc, rs,
