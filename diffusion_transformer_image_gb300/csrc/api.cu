@@ -513,12 +513,15 @@ dit_status dit_denoise_step(const dit_model_config* cfg, const dit_model_weights
     p.vec = w->out_b;
     if (launch_gemm(EPI_F32_BIAS, 0, bws.a, H, w->out_w, H, p, st) != cudaSuccess)
       return DIT_ECUDA;
+    // the low half completes v and applies the Euler update in its epilogue:
+    // latent += (sigma_next - sigma) v
     p.vec = nullptr;
-    if (launch_gemm(EPI_RESIDUAL, 0, ws.fin_lo, H, w->out_w, H, p, st) != cudaSuccess)
+    p.aux = latent;
+    p.scalar = sigma_next - sigma;
+    if (launch_gemm(EPI_EULER, 0, ws.fin_lo, H, w->out_w, H, p, st) != cudaSuccess)
       return DIT_ECUDA;
   }
-  const float dt = sigma_next - sigma;
-  return cuda_status(launch_euler(latent, v, (long long)n_img * C, dt, st));
+  return DIT_OK;
 }
 
 dit_status flowmatch_euler_step(float* x, const float* v, int64_t n, float sigma,

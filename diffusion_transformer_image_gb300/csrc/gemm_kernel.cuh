@@ -20,6 +20,10 @@
 //   EPI_SWIGLU    h = SiLU(gate) * up, gate and up columns in one tile
 //   EPI_GEGLU     the same with the clamped tanh GELU ([ERNIE] section V, Bug 1)
 //   EPI_RESIDUAL_TANH / _SIGMOID  x += f(gate) * y ([ZFLOW] sections IV, V)
+//   EPI_EULER     the second (low-half) pass of the output projection: the
+//                 velocity v = out + y is completed and the flow-matching Euler
+//                 update latent += (sigma_next - sigma) v applied, the product
+//                 rounded before the add ([ZFLOW] section IV, Euler sign +1)
 //   EPI_QKV       per-head LayerNorm of q and k with gain/bias, then RoPE;
 //                 q and k written head-major, v transposed per sequence, the
 //                 layouts the attention kernel loads as contiguous tiles
@@ -295,6 +299,24 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const CUtenso
       } else {
         for (int i = 0; i < 32 && col + i < p.N; ++i)
           dst[i] = v[i] + (p.vec ? __ldg(p.vec + col + i) : 0.0f);
+      }
+    }
+  } else if constexpr (EPI == EPI_EULER) {
+#pragma unroll 1
+    for (int c = 0; c < BN / 32; ++c) {
+      const int col = n_blk * BN + c * 32;
+      if (col >= p.N) break;
+      float v[32];
+      __syncwarp();
+      tmem_ld32(tbase + c * 32, v);
+      if (!row_ok) continue;  // the loads above stay warp-uniform
+      if constexpr (F8) scale_cols(v, rs, p.sb, col, p.N);
+      float* vel = reinterpret_cast<float*>(p.out) + (size_t)row * p.ldo + col;
+      float* lat = p.aux + (size_t)row * p.ldo + col;
+      for (int i = 0; i < 32 && col + i < p.N; ++i) {
+        const float vv = __fadd_rn(vel[i], v[i]);
+        vel[i] = vv;
+        lat[i] = __fadd_rn(lat[i], __fmul_rn(p.scalar, vv));
       }
     }
   } else if constexpr (EPI == EPI_SWIGLU || EPI == EPI_GEGLU) {
@@ -608,6 +630,9 @@ cudaError_t launch_gemm_t(int epi, int hd, const void* A, long long lda, const v
     case EPI_RESIDUAL_TANH: return launch_impl<EPI_RESIDUAL_TANH, 0, F8>(ta, tb, to, p, grid, st);
     case EPI_RESIDUAL_SIGMOID:
       return launch_impl<EPI_RESIDUAL_SIGMOID, 0, F8>(ta, tb, to, p, grid, st);
+    case EPI_EULER:
+      if constexpr (!F8) return launch_impl<EPI_EULER, 0, F8>(ta, tb, to, p, grid, st);
+      return cudaErrorInvalidValue;
     case EPI_QKV:
       if (hd == 64) return launch_impl<EPI_QKV, 64, F8>(ta, tb, to, p, grid, st);
       if (hd == 128) return launch_impl<EPI_QKV, 128, F8>(ta, tb, to, p, grid, st);

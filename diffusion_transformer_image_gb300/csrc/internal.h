@@ -40,7 +40,8 @@ enum GemmEpi : int {
   EPI_QKV = 4,        // qk-norm + RoPE -> qk buffer; v -> transposed buffer
   EPI_GEGLU = 5,      // out bf16 = gelu_tanh_clamped(acc_gate) * acc_up
   EPI_RESIDUAL_TANH = 6,     // out fp32 += tanh(gate) * acc
-  EPI_RESIDUAL_SIGMOID = 7   // out fp32 += sigmoid(gate) * acc
+  EPI_RESIDUAL_SIGMOID = 7,  // out fp32 += sigmoid(gate) * acc
+  EPI_EULER = 8              // v = out + acc (out fp32, rewritten); aux += scalar * v
 };
 
 struct QkvEpi {
@@ -64,6 +65,8 @@ struct GemmParams {
   const float* vec;     // bias (EPI_F32_BIAS) or gate (EPI_RESIDUAL), may be null
   const float* sa;      // e4m3 GEMM: scale of each A row [M]
   const float* sb;      // e4m3 GEMM: scale of each B row [N] (GLU: [2N])
+  float* aux;           // EPI_EULER: the latent [M, ldo] updated in place
+  float scalar;         // EPI_EULER: sigma_next - sigma
   QkvEpi qkv;
   DevErr err;
 };

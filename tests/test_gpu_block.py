@@ -322,6 +322,29 @@ def test_denoise_step_tiny(step):
     assert cosine(lat, new_ref) >= 0.999
 
 
+def test_denoise_euler_fused_bit_exact():
+    """The output projection's second pass applies the Euler update in its
+    epilogue: the new latent equals latent + (sigma_next - sigma) v exactly,
+    v being the velocity the step returns, the product rounded before the add
+    (float32 arithmetic in numpy, which does not fuse)."""
+    wl = TINY_DIT
+    s = O.flowmatch_sigmas(8, 4.0)
+    sig, sig_n = float(s[2]), float(s[3])
+    mw = synth.model_weights(wl, seed=0, n_layers=2)
+    cfg = dit.model_config_from(wl, 2)
+    model = dit.DeviceModel(mw, dev())
+    lat0 = synth.latent_input(wl, seed=1).to(dev()).contiguous()
+    lat = lat0.clone()
+    v = torch.empty_like(lat)
+    dit.dit_denoise_step(cfg, model, lat, synth.text_input(wl, seed=1).to(dev()), wl.grid_h,
+                         wl.grid_w, sig, sig_n, velocity_out=v)
+    torch.cuda.synchronize()
+    assert dit.dit_last_device_error() == dit.DIT_OK
+    dt = np.float32(sig_n) - np.float32(sig)
+    want = (npf(lat0) + dt * npf(v)).astype(np.float32)
+    np.testing.assert_array_equal(npf(lat), want)
+
+
 def test_whole_loop_cuda_graph_matches_eager():
     """All 8 Euler steps of a small denoiser captured in one CUDA graph (the
     library allocates nothing and never synchronises, so the path captures);
