@@ -77,3 +77,56 @@ def test_workspace_sizes(dit):
     assert dit.lib.dit_denoise_workspace_bytes(ctypes.byref(m), 64, 64, 256) > ws
     m.rope_axes[0] = 30   # axes no longer sum to head_dim
     assert dit.lib.dit_denoise_workspace_bytes(ctypes.byref(m), 64, 64, 256) == 0
+
+
+def test_w8a8_workspace_and_shape_limits(dit):
+    n = 4352
+    bf16 = dit.block_config(4096, 32, 32, 128, 12288)
+    w8 = dit.block_config(4096, 32, 32, 128, 12288, linear_format="w8a8_h256")
+    ws16 = dit.lib.dit_block_workspace_bytes(ctypes.byref(bf16), n, 1)
+    ws8 = dit.lib.dit_block_workspace_bytes(ctypes.byref(w8), n, 1)
+    # e4m3 codes of a, o, h (1 byte each) and three row-scale vectors
+    extra = n * (4096 + 4096 + 12288) + 3 * 4 * n
+    assert extra <= ws8 - ws16 <= extra + 6 * 256
+    # the Hadamard blocks need multiples of 256 along every contraction
+    for args in ((4096 + 64, 32, 32, 128, 12288),    # hidden
+                 (4096, 30, 30, 128, 12288),         # n_heads * d = 3840 is fine ...
+                 (4096, 32, 32, 128, 12288 + 128)):  # ffn
+        c = dit.block_config(*args, linear_format="w8a8_h256")
+        ok = args[0] % 256 == 0 and (args[1] * args[3]) % 256 == 0 and args[4] % 256 == 0
+        assert (dit.lib.dit_block_workspace_bytes(ctypes.byref(c), n, 1) > 0) == ok
+    too_wide = dit.block_config(4096, 32, 32, 128, 16384 + 256, linear_format="w8a8_h256")
+    assert dit.lib.dit_block_workspace_bytes(ctypes.byref(too_wide), n, 1) == 0
+    bad_fmt = dit.block_config(4096, 32, 32, 128, 12288)
+    bad_fmt.linear_format = 2
+    assert dit.lib.dit_block_workspace_bytes(ctypes.byref(bad_fmt), n, 1) == 0
+
+
+def test_w8a8_entry_points_reject_bad_arguments_on_host(dit):
+    p = ctypes.c_void_p(4096)  # a 16-byte-aligned stand-in, never dereferenced
+    s = None
+    # rows not a multiple of 256 columns, or too long, or a misaligned stride
+    assert dit.lib.dit_rotate_quantize(p, 300, 4, 300, p, 304, p, s) == dit.DIT_EINVAL
+    assert dit.lib.dit_rotate_quantize(p, 32768, 4, 32768, p, 32768, p, s) == dit.DIT_EUNSUPPORTED
+    assert dit.lib.dit_rotate_quantize(p, 1028, 4, 1024, p, 1024, p, s) == dit.DIT_EINVAL
+    assert dit.lib.dit_ln_modulate_rotate_quantize(4, p, 4096, 4, 4096, p, p, 1e-6, p, 4096, p,
+                                                   s) == dit.DIT_EINVAL
+    assert dit.lib.dit_ln_modulate_rotate_quantize(0, p, 8448, 4, 8448, p, p, 1e-6, p, 8448, p,
+                                                   s) == dit.DIT_EUNSUPPORTED
+    # e4m3 linear: missing scales, K not a multiple of 16
+    assert dit.lib.dit_linear_e4m3(dit.DIT_EPI_BF16, p, None, 64, p, p, 64, 4, 4, 64, p, 8, None,
+                                   s) == dit.DIT_EINVAL
+    assert dit.lib.dit_linear_e4m3(dit.DIT_EPI_BF16, p, p, 72, p, p, 72, 4, 4, 72, p, 8, None,
+                                   s) == dit.DIT_EINVAL
+    # the e4m3 QKV entry wants the W8A8 format; the bf16 one refuses it
+    cfg16 = dit.block_config(4096, 32, 32, 128, 12288)
+    cfg8 = dit.block_config(4096, 32, 32, 128, 12288, linear_format="w8a8_h256")
+    w = dit.BlockWeights(*([4096] * len(dit.BlockWeights._fields_)))
+    assert dit.lib.dit_qkv_rope_e4m3(ctypes.byref(cfg16), ctypes.byref(w), p, p, 256, 1, p, p, p,
+                                     p, s) == dit.DIT_EINVAL
+    assert dit.lib.dit_qkv_rope(ctypes.byref(cfg8), ctypes.byref(w), p, 256, 1, p, p, p, p,
+                                s) == dit.DIT_EUNSUPPORTED
+    # a W8A8 block without weight scales
+    w.w_qkv_scale = None
+    assert dit.lib.dit_block_forward(ctypes.byref(cfg8), ctypes.byref(w), p, 256, 1, p, p, p, p,
+                                     1 << 30, s) == dit.DIT_EINVAL
