@@ -374,9 +374,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           pk[c / 2] = pack_bf16x2(e0, e1);
         }
         __syncwarp();
-        tmem_st16u(s_tmem + half * (HC / 2) + ch * 16, pk);
+        tmem_st16u_nowait(s_tmem + half * (HC / 2) + ch * 16, pk);
       }
       l += ((r8[0] + r8[1]) + (r8[2] + r8[3])) + ((r8[4] + r8[5]) + (r8[6] + r8[7]));
+      tmem_wait_st();  // both chunks of P are in TMEM before the MMA may read them
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars->p_full[t]);
