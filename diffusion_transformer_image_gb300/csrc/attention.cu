@@ -361,22 +361,25 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
       // P_t(j) in bf16, two per 32-bit column, into the first half of S_t's
       // columns: this half's 64 keys land in columns [32 half, 32 half + 32).
-      float r8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      // exponent arguments and row sums two at a time (packed fp32: each lane
+      // rounds exactly like the scalar fmaf / add)
+      float2 r4[4] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};
+      const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
+      const float2 nm2 = make_float2(-m_used, -m_used);
 #pragma unroll
       for (int ch = 0; ch < HC / 32; ++ch) {
         uint32_t pk[16];
 #pragma unroll
         for (int c = 0; c < 32; c += 2) {
-          const float e0 = ex2_approx(fmaf(s[ch * 32 + c], p.scale_log2, -m_used));
-          const float e1 = ex2_approx(fmaf(s[ch * 32 + c + 1], p.scale_log2, -m_used));
-          r8[c & 7] += e0;
-          r8[(c + 1) & 7] += e1;
-          pk[c / 2] = pack_bf16x2(e0, e1);
+          const float2 x = __ffma2_rn(make_float2(s[ch * 32 + c], s[ch * 32 + c + 1]), sc2, nm2);
+          const float2 e = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+          r4[(c >> 1) & 3] = __fadd2_rn(r4[(c >> 1) & 3], e);
+          pk[c / 2] = pack_bf16x2(e.x, e.y);
         }
         __syncwarp();
         tmem_st16u_nowait(s_tmem + half * (HC / 2) + ch * 16, pk);
       }
-      l += ((r8[0] + r8[1]) + (r8[2] + r8[3])) + ((r8[4] + r8[5]) + (r8[6] + r8[7]));
+      l += ((r4[0].x + r4[0].y) + (r4[1].x + r4[1].y)) + ((r4[2].x + r4[2].y) + (r4[3].x + r4[3].y));
       tmem_wait_st();  // both chunks of P are in TMEM before the MMA may read them
       tc_fence_before();
       __syncwarp();
