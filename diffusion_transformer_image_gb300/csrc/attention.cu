@@ -322,13 +322,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         for (int c = 0; c < HC; ++c)
           if (kv0 + c >= p.s_len) s[c] = -CUDART_INF_F;
       }
+      // row maximum of this half: chain i takes s[i], s[i + 8], ..., s[i + 56]
+      // with three-input maxima
+      static_assert(HC == 64, "eight chains of eight scores");
       float m8[8];
 #pragma unroll
-      for (int c = 0; c < 8; ++c) m8[c] = s[c];
-#pragma unroll
-      for (int c = 8; c < HC; ++c) m8[c & 7] = fmaxf(m8[c & 7], s[c]);
-      const float lmax = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
-                               fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+      for (int i = 0; i < 8; ++i) {
+        m8[i] = fmax3(s[i], s[i + 8], s[i + 16]);
+        m8[i] = fmax3(m8[i], s[i + 24], s[i + 32]);
+        m8[i] = fmax3(m8[i], s[i + 40], s[i + 48]);
+        m8[i] = fmaxf(m8[i], s[i + 56]);
+      }
+      const float lmax = fmaxf(fmax3(m8[0], m8[1], m8[2]),
+                               fmax3(fmax3(m8[3], m8[4], m8[5]), m8[6], m8[7]));
       // The exchange also orders the two halves' reads of S_t before either
       // overwrites S_t's columns with P_t below.  Maxima alternate between
       // two slots, so one meeting per block suffices: a slot is rewritten
