@@ -248,6 +248,36 @@ def test_invalid_arguments_enqueue_nothing():
     assert e.value.status in (dit.DIT_EUNSUPPORTED, dit.DIT_EINVAL)
 
 
+def test_empty_inputs():
+    """Zero rows or elements enqueue nothing and leave the buffers alone; an
+    empty token sequence or an empty GEMM is rejected before any launch."""
+    H = 1024
+    x = torch.randn(4, H, device=dev())
+    out = torch.full((4, H), 7.0, dtype=torch.bfloat16, device=dev())
+    p = torch.zeros(H, device=dev())
+    dit.dit_ln_modulate(0, x[:0], p, p, 1e-6, out[:0])
+    xb = x.to(torch.bfloat16)
+    codes = torch.full((4, H), 3, dtype=torch.uint8, device=dev())
+    scales = torch.full((4,), 5.0, device=dev())
+    dit.dit_rotate_quantize(xb[:0], codes[:0], scales[:0])
+    dit.dit_ln_modulate_rotate_quantize(0, x[:0], p, p, 1e-6, codes[:0], scales[:0])
+    v = torch.randn(16, device=dev())
+    xe = torch.full((16,), 0.5, device=dev())
+    dit.flowmatch_euler_step(xe[:0], v[:0], 1.0, 0.5)
+    torch.cuda.synchronize()
+    assert dit.dit_last_device_error() == dit.DIT_OK
+    assert torch.all(out == 7.0) and torch.all(codes == 3) and torch.all(scales == 5.0)
+    assert torch.all(xe == 0.5)
+    with pytest.raises(dit.DitError) as e:
+        dit.dit_linear(dit.DIT_EPI_BF16, xb[:0], xb, out[:0])
+    assert e.value.status == dit.DIT_EINVAL
+    cfg = dit.block_config(256, 4, 4, 64, 768)
+    with pytest.raises(dit.DitError) as e:
+        dit.dit_block_forward(cfg, None, x[:0, :256], None, x, x,
+                              ws=torch.zeros(256, dtype=torch.uint8, device=dev()))
+    assert e.value.status == dit.DIT_EINVAL
+
+
 # ------------------------------------------------------------- variants
 @pytest.mark.parametrize("rows,H,affine", [(37, 256, False), (130, 4096, False), (69, 1024, True)])
 def test_rms_modulate(rows, H, affine):
