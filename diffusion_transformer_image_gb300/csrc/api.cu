@@ -527,6 +527,7 @@ dit_status dit_denoise_step(const dit_model_config* cfg, const dit_model_weights
 dit_status flowmatch_euler_step(float* x, const float* v, int64_t n, float sigma,
                                 float sigma_next, void* stream) {
   if (n < 0 || (n > 0 && (!x || !v || !aligned16(x) || !aligned16(v)))) return DIT_EINVAL;
+  if (n == 0) return DIT_OK;  // nothing to do; the pointers are not read
   if (!device_state()) return DIT_ECUDA;
   return cuda_status(launch_euler(x, v, n, sigma_next - sigma, static_cast<cudaStream_t>(stream)));
 }
@@ -607,11 +608,13 @@ dit_status dit_linear_e4m3(int32_t epilogue, const void* a, const float* a_scale
 
 dit_status dit_rotate_quantize(const void* x, int64_t ldx, int32_t rows, int32_t K, void* codes,
                                int64_t ldq, float* scales, void* stream) {
-  if (!x || !codes || !scales || rows < 0 || K <= 0) return DIT_EINVAL;
-  if (K % 256 || ldx < K || ldq < K || ldx % 8 || ldq % 16 || !aligned16(x) ||
-      !aligned16(codes) || (reinterpret_cast<uintptr_t>(scales) & 3u))
+  if (rows < 0 || K <= 0 || K % 256 || ldx < K || ldq < K || ldx % 8 || ldq % 16)
     return DIT_EINVAL;
   if (K > ROTQ_MAX_K) return DIT_EUNSUPPORTED;
+  if (rows == 0) return DIT_OK;  // nothing to do; the pointers are not read
+  if (!x || !codes || !scales || !aligned16(x) || !aligned16(codes) ||
+      (reinterpret_cast<uintptr_t>(scales) & 3u))
+    return DIT_EINVAL;
   if (!device_state()) return DIT_ECUDA;
   return cuda_status(launch_rotate_quant(static_cast<const __nv_bfloat16*>(x), ldx, rows, K,
                                          static_cast<uint8_t*>(codes), ldq, scales,
@@ -622,13 +625,14 @@ dit_status dit_ln_modulate_rotate_quantize(int32_t mode, const float* x, int64_t
                                            int32_t rows, int32_t H, const float* p0,
                                            const float* p1, float eps, void* codes,
                                            int64_t ldq, float* scales, void* stream) {
-  if (mode < 0 || mode > 3 || !x || !p0 || !p1 || !codes || !scales || rows < 0 || H <= 0)
-    return DIT_EINVAL;
-  if (H % 256 || ldx < H || ldq < H || ldx % 4 || ldq % 16 || !aligned16(x) ||
-      !aligned16(p0) || !aligned16(p1) || !aligned16(codes) ||
-      (reinterpret_cast<uintptr_t>(scales) & 3u) || !(eps >= 0.0f))
+  if (mode < 0 || mode > 3 || rows < 0 || H <= 0 || H % 256 || ldx < H || ldq < H || ldx % 4 ||
+      ldq % 16 || !(eps >= 0.0f))
     return DIT_EINVAL;
   if (H > ROTQ_LN_MAX_H) return DIT_EUNSUPPORTED;
+  if (rows == 0) return DIT_OK;  // nothing to do; the pointers are not read
+  if (!x || !p0 || !p1 || !codes || !scales || !aligned16(x) || !aligned16(p0) ||
+      !aligned16(p1) || !aligned16(codes) || (reinterpret_cast<uintptr_t>(scales) & 3u))
+    return DIT_EINVAL;
   if (!device_state()) return DIT_ECUDA;
   return cuda_status(launch_ln_rotate_quant(mode, x, ldx, rows, H, p0, p1, eps,
                                             static_cast<uint8_t*>(codes), ldq, scales,
@@ -693,9 +697,11 @@ dit_status dit_attention(const dit_block_config* cfg, const void* qk, const void
 
 dit_status dit_ln_modulate(int32_t mode, const float* x, int64_t ldx, int32_t rows, int32_t H,
                            const float* p0, const float* p1, float eps, void* out, void* stream) {
-  if (mode < 0 || mode > 3 || !x || !p0 || !p1 || !out || rows < 0 || H <= 0) return DIT_EINVAL;
+  if (mode < 0 || mode > 3 || rows < 0 || H <= 0) return DIT_EINVAL;
   if (H % 4 || ldx < H || ldx % 4) return DIT_EINVAL;
   if (H > 8192) return DIT_EUNSUPPORTED;
+  if (rows == 0) return DIT_OK;  // nothing to do; the pointers are not read
+  if (!x || !p0 || !p1 || !out) return DIT_EINVAL;
   if (!aligned16(x) || !aligned16(p0) || !aligned16(p1) || !aligned16(out)) return DIT_EINVAL;
   return cuda_status(launch_ln_modulate(mode, x, ldx, rows, H, p0, p1, eps,
                                         static_cast<__nv_bfloat16*>(out), H,

@@ -28,8 +28,10 @@
  *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  All
  *     work is enqueued asynchronously on it.
  *   - Empty inputs: the row-wise entry points (norms, coding, Euler) accept
- *     zero rows or elements and enqueue nothing; a block, a denoise step, an
- *     attention call or a linear with zero tokens or rows returns DIT_EINVAL.
+ *     zero rows or elements, with any pointers (NULL included), check their
+ *     scalar arguments and return DIT_OK without enqueuing anything; a block,
+ *     a denoise step, an attention call or a linear with zero tokens or rows
+ *     returns DIT_EINVAL.
  *   - Errors: invalid arguments return DIT_EINVAL and enqueue nothing; shapes
  *     outside the kernel set return DIT_EUNSUPPORTED; a failed launch returns
  *     DIT_ECUDA.  Kernels never trap: every wait inside a kernel is bounded,

@@ -130,3 +130,23 @@ def test_w8a8_entry_points_reject_bad_arguments_on_host(dit):
     w.w_qkv_scale = None
     assert dit.lib.dit_block_forward(ctypes.byref(cfg8), ctypes.byref(w), p, 256, 1, p, p, p, p,
                                      1 << 30, s) == dit.DIT_EINVAL
+
+
+def test_empty_inputs_on_host(dit):
+    # zero rows: scalar arguments checked, pointers not read, nothing enqueued
+    # (these return before any CUDA call, so they run without a GPU)
+    L = dit.lib
+    assert L.dit_ln_modulate(0, None, 1024, 0, 1024, None, None, 1e-6, None, None) == dit.DIT_OK
+    assert L.dit_ln_modulate(0, None, 1024, 0, 1022, None, None, 1e-6, None, None) == dit.DIT_EINVAL
+    assert L.dit_ln_modulate(0, None, 1024, -1, 1024, None, None, 1e-6, None, None) == dit.DIT_EINVAL
+    assert L.dit_rotate_quantize(None, 1024, 0, 1024, None, 1024, None, None) == dit.DIT_OK
+    assert L.dit_rotate_quantize(None, 1024, 0, 1000, None, 1024, None, None) == dit.DIT_EINVAL
+    assert L.dit_ln_modulate_rotate_quantize(0, None, 1024, 0, 1024, None, None, 1e-6, None, 1024,
+                                             None, None) == dit.DIT_OK
+    assert L.flowmatch_euler_step(None, None, 0, 1.0, 0.5, None) == dit.DIT_OK
+    assert L.flowmatch_euler_step(None, None, -1, 1.0, 0.5, None) == dit.DIT_EINVAL
+    # an empty GEMM or token sequence is an error
+    assert L.dit_linear(dit.DIT_EPI_BF16, None, 64, None, 64, 0, 64, 64, None, 64, None,
+                        None) == dit.DIT_EINVAL
+    cfg = dit.block_config(256, 4, 4, 64, 768)
+    assert L.dit_block_workspace_bytes(ctypes.byref(cfg), 0, 1) == 0
