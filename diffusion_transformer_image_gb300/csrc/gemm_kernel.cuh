@@ -2,12 +2,20 @@
 // template; gemm.cu launches the bf16 instances, gemm_f8.cu the e4m3 ones).
 //
 // D[M, N] = A[M, K] B[N, K]^T: bf16 operands staged in shared memory by TMA
-// (128-byte swizzle), 128 x 256 x 64 tiles, fp32 accumulators in tensor
-// memory, double-buffered so that the epilogue of one tile overlaps the
-// main loop of the next.  Roles per CTA (192 threads, one CTA per SM):
-//   warp 0      TMA producer (one lane)
-//   warp 1      TMEM allocator and MMA issuer (one lane)
-//   warps 2..5  epilogue: thread t of the group owns accumulator row t
+// (128-byte swizzle), fp32 accumulators in tensor memory, double-buffered so
+// that the epilogue of one tile overlaps the main loop of the next.  A cluster
+// of two CTAs (on two SMs) computes one 256 x 256 tile with tcgen05 pair MMAs
+// (cta_group::2): each CTA stages its 128 rows of A and 128 of the tile's 256
+// rows of B, 64 values of K per stage, so a stage is 32 KB per SM (a single
+// CTA's 128 x 256 tile would need 48 KB for the same MMA work per SM) and six
+// stages fit.  Rank 0 of the pair issues the MMAs for both; each CTA's tensor
+// memory holds the 128 accumulator rows of its half.  Roles per CTA (192
+// threads, one CTA per SM):
+//   warp 0      TMA producer (one lane); both CTAs' copies complete on rank 0's
+//               stage barrier
+//   warp 1      TMEM allocator (both CTAs) and MMA issuer (one lane of rank 0)
+//   warps 2..5  epilogue: thread t of the group owns accumulator row t of its
+//               CTA's half
 //
 // The epilogues are the fused pointwise tails of the block's linears
 // ([ZFLOW] "From Python + CUDA to Pure Rust + Metal 4", section VI: fused
@@ -39,10 +47,13 @@ namespace dit {
 namespace {
 
 // One pipeline stage holds 128 bytes of K per operand row: 64 bf16 or 128
-// e4m3 values, the same 128-byte swizzled layout either way.
-constexpr int BM = 128, BN = 256, BK_BYTES = 128, STAGES = 4;
+// e4m3 values, the same 128-byte swizzled layout either way.  BM rows of A
+// and BNH rows of B per CTA; PM x BN output rows x columns per CTA pair.
+constexpr int BM = 128, BN = 256, BK_BYTES = 128, STAGES = 6;
+constexpr int PM = 2 * BM;
+constexpr int BNH = BN / 2;
 constexpr int A_BYTES = BM * BK_BYTES;
-constexpr int B_BYTES = BN * BK_BYTES;
+constexpr int B_BYTES = BNH * BK_BYTES;
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int TMEM_COLS = 2 * BN;
 constexpr int NUM_THREADS = 192;
@@ -427,10 +438,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                                                (is_staged<EPI>() ? EPI_SMEM : 0));
 
   const int warp = warp_id(), lane = lane_id();
+  const uint32_t rank = cluster_rank();  // 0 issues the pair's MMAs
+  const int pair = (int)cluster_index(), num_pairs = (int)cluster_count();
   const int num_tiles = p.num_m * p.num_n;
   constexpr int BK = F8 ? BK_BYTES : BK_BYTES / 2;  // K elements per stage
   const int k_blocks = (p.K + BK - 1) / BK;
 
+  // Barriers, the same layout in both CTAs.  Used on rank 0 only: full (both
+  // CTAs' copies of a stage), tempty (both CTAs' epilogue warps), drain.
+  // Used on both: empty and tfull, which rank 0's commits signal in both.
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&bars->full[s], 1);
@@ -438,7 +454,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&bars->tfull[a], 1);
-      mbar_init(&bars->tempty[a], 4);
+      mbar_init(&bars->tempty[a], 8);
     }
     mbar_init(&bars->drain, 1);
     fence_barrier_init();
@@ -446,11 +462,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     tma_prefetch_desc(&tmB);
   }
   if (warp == 1) {
-    tmem_alloc(&bars->tmem_slot, TMEM_COLS);
-    tmem_relinquish();
+    tmem_alloc_pair(&bars->tmem_slot, TMEM_COLS);
+    tmem_relinquish_pair();
   }
   tc_fence_before();
   __syncthreads();
+  cluster_sync();  // both CTAs' barriers exist before either signals the other
   tc_fence_after();
   const uint32_t tmem_base = bars->tmem_slot;
 
@@ -460,8 +477,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       int stage = 0;
       uint32_t phase = 0, filled = 0, fill_parity = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+      for (int t = pair; t < num_tiles && ok; t += num_pairs) {
         const int m_blk = t % p.num_m, n_blk = t / p.num_m;
+        const int a_row = m_blk * PM + (int)rank * BM;
+        // GLU tiles: rank 0 stages the 128 gate rows, rank 1 the matching up rows
+        const int b_row = (EPI == EPI_SWIGLU || EPI == EPI_GEGLU)
+                              ? (rank ? p.N : 0) + n_blk * BNH
+                              : n_blk * BN + (int)rank * BNH;
         for (int kb = 0; kb < k_blocks; ++kb) {
           if (!mbar_wait(&bars->empty[stage], phase ^ 1u, p.err)) {
             ok = false;
@@ -469,38 +491,38 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
           uint8_t* sa = smem + (size_t)stage * STAGE_BYTES;
           uint8_t* sb = sa + A_BYTES;
-          mbar_arrive_expect_tx(&bars->full[stage], STAGE_BYTES);
-          tma_load_2d(sa, &tmA, &bars->full[stage], kb * BK, m_blk * BM);
-          if constexpr (EPI == EPI_SWIGLU || EPI == EPI_GEGLU) {
-            tma_load_2d(sb, &tmB, &bars->full[stage], kb * BK, n_blk * 128);
-            tma_load_2d(sb + B_BYTES / 2, &tmB, &bars->full[stage], kb * BK, p.N + n_blk * 128);
-          } else {
-            tma_load_2d(sb, &tmB, &bars->full[stage], kb * BK, n_blk * BN);
+          if (rank == 0) {
+            mbar_arrive_expect_tx(&bars->full[stage], 2 * STAGE_BYTES);
+            filled |= 1u << stage;
+            fill_parity = (fill_parity & ~(1u << stage)) | (phase << stage);
           }
-          filled |= 1u << stage;
-          fill_parity = (fill_parity & ~(1u << stage)) | (phase << stage);
+          const uint32_t fb = mapa_shared(smem_u32(&bars->full[stage]), 0);
+          tma_load_2d_pair(sa, &tmA, fb, kb * BK, a_row);
+          tma_load_2d_pair(sb, &tmB, fb, kb * BK, b_row);
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
           }
         }
       }
-      // Every copy issued must have landed before the CTA may exit.
-      for (int s = 0; s < STAGES; ++s)
-        if (filled & (1u << s)) mbar_wait(&bars->full[s], (fill_parity >> s) & 1u, p.err);
+      // Every copy issued must have landed before the CTAs may exit (rank 0's
+      // stage barriers count both CTAs' copies).
+      if (rank == 0)
+        for (int s = 0; s < STAGES; ++s)
+          if (filled & (1u << s)) mbar_wait(&bars->full[s], (fill_parity >> s) & 1u, p.err);
     }
   } else if (warp == 1) {
-    if (lane == 0) {
+    if (lane == 0 && rank == 0) {
       // ------------------------------------------------ MMA issuer
-      constexpr uint32_t idesc = F8 ? idesc_e4m3_f32(BM, BN) : idesc_bf16_f32(BM, BN);
+      constexpr uint32_t idesc = F8 ? idesc_e4m3_f32(PM, BN) : idesc_bf16_f32(PM, BN);
       int stage = 0;
       uint32_t phase = 0;
       int local = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x, ++local) {
+      for (int t = pair; t < num_tiles && ok; t += num_pairs, ++local) {
         const int acc = local & 1;
         const uint32_t acc_phase = (local >> 1) & 1;
-        if (!mbar_wait(&bars->tempty[acc], acc_phase ^ 1u, p.err)) break;
+        if (!mbar_wait_cluster(&bars->tempty[acc], acc_phase ^ 1u, p.err)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
         for (int kb = 0; kb < k_blocks; ++kb) {
@@ -515,22 +537,22 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
           for (int k = 0; k < BK_BYTES / 32; ++k) {
             if constexpr (F8)
-              umma_e4m3(d_tmem, sdesc_sw128(a_addr + k * 32), sdesc_sw128(b_addr + k * 32),
-                        idesc, (kb | k) != 0);
+              umma_e4m3_pair(d_tmem, sdesc_sw128(a_addr + k * 32), sdesc_sw128(b_addr + k * 32),
+                             idesc, (kb | k) != 0);
             else
-              umma_bf16(d_tmem, sdesc_sw128(a_addr + k * 32), sdesc_sw128(b_addr + k * 32),
-                        idesc, (kb | k) != 0);
+              umma_bf16_pair(d_tmem, sdesc_sw128(a_addr + k * 32), sdesc_sw128(b_addr + k * 32),
+                             idesc, (kb | k) != 0);
           }
-          umma_commit(&bars->empty[stage]);
+          umma_commit_pair_both(&bars->empty[stage]);
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
           }
         }
-        if (ok) umma_commit(&bars->tfull[acc]);
+        if (ok) umma_commit_pair_both(&bars->tfull[acc]);
       }
       // All MMAs issued must complete before TMEM is released.
-      umma_commit(&bars->drain);
+      umma_commit_pair_self(&bars->drain);
       mbar_wait(&bars->drain, 0, p.err);
     }
   } else {
@@ -538,51 +560,78 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int quarter = warp & 3;  // TMEM lanes [32 quarter, 32 quarter + 32)
     const int r_in = quarter * 32 + lane;
     EpiStage es{smem + (size_t)STAGES * STAGE_BYTES + (size_t)quarter * 2 * EBUF_BYTES, 0};
+    const uint32_t te0 = mapa_shared(smem_u32(&bars->tempty[0]), 0);  // rank 0's barriers
+    const uint32_t te1 = mapa_shared(smem_u32(&bars->tempty[1]), 0);
     int local = 0;
-    for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++local) {
+    for (int t = pair; t < num_tiles; t += num_pairs, ++local) {
       const int m_blk = t % p.num_m, n_blk = t / p.num_m;
       const int acc = local & 1;
       const uint32_t acc_phase = (local >> 1) & 1;
       if (!mbar_wait(&bars->tfull[acc], acc_phase, p.err)) break;
       tc_fence_after();
       const uint32_t tbase = tmem_base + (uint32_t)(acc * BN) + ((uint32_t)(quarter * 32) << 16);
-      epilogue_tile<EPI, HD, F8>(p, &tmO, es, tbase, m_blk * BM + r_in, m_blk * BM + quarter * 32,
+      const int row_base = m_blk * PM + (int)rank * BM;
+      epilogue_tile<EPI, HD, F8>(p, &tmO, es, tbase, row_base + r_in, row_base + quarter * 32,
                                  lane, n_blk);
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->tempty[acc]);
+      if (lane == 0) mbar_arrive_cluster(acc ? te1 : te0);
     }
     if (lane == 0) bulk_wait<0>();  // every staged store has completed
   }
 
   tc_fence_before();
   __syncthreads();
+  cluster_sync();  // neither CTA leaves while the pair may still touch its memory
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, TMEM_COLS);
+    tmem_dealloc_pair(tmem_base, TMEM_COLS);
   }
 }
 
+// Launches clusters of two CTAs, persistent: one pair per tile at most, and
+// no more pairs than can be resident at once (queried once per device).
 template <int EPI, int HD, bool F8>
 cudaError_t launch_impl(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& to,
-                        const GemmParams& p, int grid, cudaStream_t st) {
-  static bool attr_set[64] = {};
+                        const GemmParams& p, int tiles, int sm_count, cudaStream_t st) {
+  static int max_pairs[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev < 64 && !attr_set[dev]) {
+  if (dev >= 64) return cudaErrorInvalidDevice;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+  cfg.dynamicSmemBytes = smem_bytes<EPI>();
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (max_pairs[dev] == 0) {
     cudaError_t e = cudaFuncSetAttribute(gemm_kernel<EPI, HD, F8>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem_bytes<EPI>());
     if (e != cudaSuccess) return e;
-    attr_set[dev] = true;
+    int n = 0;
+    cfg.gridDim = dim3(2, 1, 1);
+    if (cudaOccupancyMaxActiveClusters(&n, gemm_kernel<EPI, HD, F8>, &cfg) != cudaSuccess ||
+        n <= 0) {
+      (void)cudaGetLastError();
+      n = sm_count / 2;
+    }
+    max_pairs[dev] = n < 1 ? 1 : n;
   }
-  gemm_kernel<EPI, HD, F8><<<grid, NUM_THREADS, smem_bytes<EPI>(), st>>>(ta, tb, to, p);
+  const int pairs = tiles < max_pairs[dev] ? tiles : max_pairs[dev];
+  cfg.gridDim = dim3(2 * pairs, 1, 1);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_kernel<EPI, HD, F8>, ta, tb, to, p);
   count_launch();
-  return cudaGetLastError();
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
-// Encodes the two operand maps (boxes of 128 bytes of K by 128 or 256 rows),
-// counts the tiles and launches one persistent CTA per SM at most.
+// Encodes the two operand maps (boxes of 128 bytes of K by 128 rows), counts
+// the pair tiles and launches one persistent CTA pair per two SMs at most.
 template <bool F8>
 cudaError_t launch_gemm_t(int epi, int hd, const void* A, long long lda, const void* B,
                           long long ldb, GemmParams& p, cudaStream_t st) {
@@ -602,7 +651,7 @@ cudaError_t launch_gemm_t(int epi, int hd, const void* A, long long lda, const v
     const uint64_t rows = glu ? 2ull * p.N : (uint64_t)p.N;
     const uint64_t dims[2] = {(uint64_t)p.K, rows};
     const uint64_t strides[1] = {(uint64_t)ldb * ES};
-    const uint32_t box[2] = {BK, glu ? 128u : (uint32_t)BN};
+    const uint32_t box[2] = {BK, (uint32_t)BNH};
     if (!make_tmap(&tb, ES, B, 2, dims, strides, box)) return cudaErrorInvalidValue;
   }
   // the output map of the staged epilogues (unused by the others): fp32
@@ -616,26 +665,26 @@ cudaError_t launch_gemm_t(int epi, int hd, const void* A, long long lda, const v
     const uint32_t box[2] = {resid ? 32u : 64u, 32u};
     if (!make_tmap(&to, oes, p.out, 2, dims, strides, box)) return cudaErrorInvalidValue;
   }
-  p.num_m = (p.M + BM - 1) / BM;
+  p.num_m = (p.M + PM - 1) / PM;
   p.num_n = glu ? p.N / 128 : (p.N + BN - 1) / BN;
   p.err = dev_err(ds);
   const int tiles = p.num_m * p.num_n;
-  const int grid = tiles < ds->sm_count ? tiles : ds->sm_count;
+  const int sms = ds->sm_count;
   switch (epi) {
-    case EPI_BF16: return launch_impl<EPI_BF16, 0, F8>(ta, tb, to, p, grid, st);
-    case EPI_F32_BIAS: return launch_impl<EPI_F32_BIAS, 0, F8>(ta, tb, to, p, grid, st);
-    case EPI_RESIDUAL: return launch_impl<EPI_RESIDUAL, 0, F8>(ta, tb, to, p, grid, st);
-    case EPI_SWIGLU: return launch_impl<EPI_SWIGLU, 0, F8>(ta, tb, to, p, grid, st);
-    case EPI_GEGLU: return launch_impl<EPI_GEGLU, 0, F8>(ta, tb, to, p, grid, st);
-    case EPI_RESIDUAL_TANH: return launch_impl<EPI_RESIDUAL_TANH, 0, F8>(ta, tb, to, p, grid, st);
+    case EPI_BF16: return launch_impl<EPI_BF16, 0, F8>(ta, tb, to, p, tiles, sms, st);
+    case EPI_F32_BIAS: return launch_impl<EPI_F32_BIAS, 0, F8>(ta, tb, to, p, tiles, sms, st);
+    case EPI_RESIDUAL: return launch_impl<EPI_RESIDUAL, 0, F8>(ta, tb, to, p, tiles, sms, st);
+    case EPI_SWIGLU: return launch_impl<EPI_SWIGLU, 0, F8>(ta, tb, to, p, tiles, sms, st);
+    case EPI_GEGLU: return launch_impl<EPI_GEGLU, 0, F8>(ta, tb, to, p, tiles, sms, st);
+    case EPI_RESIDUAL_TANH: return launch_impl<EPI_RESIDUAL_TANH, 0, F8>(ta, tb, to, p, tiles, sms, st);
     case EPI_RESIDUAL_SIGMOID:
-      return launch_impl<EPI_RESIDUAL_SIGMOID, 0, F8>(ta, tb, to, p, grid, st);
+      return launch_impl<EPI_RESIDUAL_SIGMOID, 0, F8>(ta, tb, to, p, tiles, sms, st);
     case EPI_EULER:
-      if constexpr (!F8) return launch_impl<EPI_EULER, 0, F8>(ta, tb, to, p, grid, st);
+      if constexpr (!F8) return launch_impl<EPI_EULER, 0, F8>(ta, tb, to, p, tiles, sms, st);
       return cudaErrorInvalidValue;
     case EPI_QKV:
-      if (hd == 64) return launch_impl<EPI_QKV, 64, F8>(ta, tb, to, p, grid, st);
-      if (hd == 128) return launch_impl<EPI_QKV, 128, F8>(ta, tb, to, p, grid, st);
+      if (hd == 64) return launch_impl<EPI_QKV, 64, F8>(ta, tb, to, p, tiles, sms, st);
+      if (hd == 128) return launch_impl<EPI_QKV, 128, F8>(ta, tb, to, p, tiles, sms, st);
       return cudaErrorInvalidValue;
     default: return cudaErrorInvalidValue;
   }
