@@ -5,8 +5,10 @@ checked against.  Only the tests, ``__graft_entry__.smoke()`` and the CPU
 baseline legs of ``bench.py`` may import it; the product library never does,
 and it imports nothing from the product package.
 
-Precision: float32 throughout, as the CPU f32 reference backend of the
-zml-flow-rs page does ("From Python + CUDA to Pure Rust + Metal 4", §X).  Every
+Precision: float32 throughout, the precision the pages fix for their own
+reference: the zml-flow-rs page's CPU f32 reference backend ("From Python +
+CUDA to Pure Rust + Metal 4", §II and §X) runs the same graphs, and block
+parity there is the bf16-vs-f32 gap.  Every
 linear is one numpy float32 matmul (a library primitive); everything else is
 written out step by step in the order the pages give it.  Inputs are the
 seeded generator's bf16 values widened to float32; no intermediate is rounded.
@@ -19,8 +21,7 @@ Sources, cited by page title and section:
   [MAKEPAD] makepad commit log for libs/ai/metal/shaders/ggml (resident
             pre-norm ViT backbone commit)
 
-Readings taken where the pages are silent or disagree (each one is listed in
-the design doc with its reason):
+Readings taken where the pages are silent or disagree:
   * every norm is LayerNorm without affine (eps 1e-6); per-head qk-LayerNorm
     has a gain and bias over head_dim;
   * qk-LayerNorm is applied before RoPE ([ZFLOW] §VI: the fused per-head norm
