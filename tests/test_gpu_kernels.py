@@ -21,7 +21,7 @@ def _rms(a):
 
 # ------------------------------------------------------------------ GEMM
 @pytest.mark.parametrize("M,N,K", [(128, 256, 64), (130, 384, 128), (300, 512, 4096),
-                                   (257, 128, 192), (1, 256, 256)])
+                                   (257, 128, 192), (1, 256, 256), (200, 320, 200)])
 def test_linear_bf16(M, N, K):
     a = bf16_normal((M, K), f"lin_a{M}_{K}")
     w = bf16_normal((N, K), f"lin_w{N}_{K}", std=0.05)
@@ -44,7 +44,7 @@ def test_linear_f32_bias(M, N, K):
 
 
 @pytest.mark.parametrize("gated", [True, False])
-@pytest.mark.parametrize("M,N,K", [(256, 512, 256), (300, 256, 1024)])
+@pytest.mark.parametrize("M,N,K", [(256, 512, 256), (300, 256, 1024), (260, 100, 136)])
 def test_linear_gated_residual(M, N, K, gated):
     a = bf16_normal((M, K), f"gr_a{M}_{K}")
     w = bf16_normal((N, K), f"gr_w{N}_{K}", std=0.05)
