@@ -150,3 +150,23 @@ def test_empty_inputs_on_host(dit):
                         None) == dit.DIT_EINVAL
     cfg = dit.block_config(256, 4, 4, 64, 768)
     assert L.dit_block_workspace_bytes(ctypes.byref(cfg), 0, 1) == 0
+
+
+def test_short_workspace_is_rejected_before_any_launch(dit):
+    # The checks read only host values: the placeholder device addresses
+    # below (16-byte aligned, never dereferenced) stand for caller buffers.
+    fake = 1 << 20
+    cfg = dit.block_config(256, 4, 4, 64, 768)
+    w = dit.BlockWeights(*([fake] * 8))   # linears and the qk-norm gains and biases
+    n = 256
+    need = dit.lib.dit_block_workspace_bytes(ctypes.byref(cfg), n, 1)
+    assert need > 0
+    st = dit.lib.dit_block_forward(ctypes.byref(cfg), ctypes.byref(w), ctypes.c_void_p(fake), n, 1,
+                                   ctypes.c_void_p(fake), ctypes.c_void_p(fake),
+                                   ctypes.c_void_p(fake), ctypes.c_void_p(fake), need - 1, None)
+    assert st == dit.DIT_EWORKSPACE
+    # a misaligned workspace is an argument error, checked first
+    st = dit.lib.dit_block_forward(ctypes.byref(cfg), ctypes.byref(w), ctypes.c_void_p(fake), n, 1,
+                                   ctypes.c_void_p(fake), ctypes.c_void_p(fake),
+                                   ctypes.c_void_p(fake), ctypes.c_void_p(fake + 8), need, None)
+    assert st == dit.DIT_EINVAL

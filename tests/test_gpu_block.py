@@ -4,6 +4,7 @@ Per-block criterion: max|err| <= 2e-2 x RMS(oracle output).  Small cases are
 compared element by element on every output; the full-size workloads are
 compared on sampled rows that the oracle computes one by one (keys and
 values from every row, everything after attention per row)."""
+import dataclasses
 import os
 
 import numpy as np
@@ -189,6 +190,86 @@ def test_block_token_permutation_equivariance():
         dit.dit_block_forward(cfg, blk, xg, mod, c, s)
         outs.append(npf(xg))
     assert_block_parity(outs[1], outs[0][perm.numpy()], frac=1e-2, what="permutation")
+
+
+def test_block_position_offset_invariance():
+    # RoPE encodes relative positions: shifting every token's position by one
+    # vector leaves a non-causal block's output unchanged (up to bf16
+    # rounding flips of q and k, far inside the bound below).
+    wl = synth.WORKLOADS["tiny_block"]
+    w = synth.block_weights(wl, 0, seed=0)
+    x = synth.residual_input(wl, seed=1)
+    mod = synth.modulation_input(wl, seed=1).to(dev())
+    cfg = dit.block_config_from(wl)
+    blk = dit.DeviceBlock(w, dev())
+    pos = torch.from_numpy(O.position_ids(wl.grid_h, wl.grid_w, wl.n_txt))
+    deltas = []
+    for off in ((0, 0, 0), (5, 3, 11)):
+        p = (pos + torch.tensor(off, dtype=torch.int32)).contiguous().to(dev())
+        c = torch.empty(wl.n_tokens, wl.head_dim // 2, device=dev())
+        s = torch.empty_like(c)
+        dit.dit_rope_table_pos(p, wl.rope_axes, wl.rope_theta, c, s)
+        xg = x.to(dev()).contiguous()
+        dit.dit_block_forward(cfg, blk, xg, mod, c, s)
+        deltas.append(npf(xg) - npf(x))
+    torch.cuda.synchronize()
+    assert dit.dit_last_device_error() == dit.DIT_OK
+    assert_block_parity(deltas[1], deltas[0], frac=2e-2, what="position offset")
+
+
+def test_gqa_equals_mha_with_repeated_kv_heads():
+    # Query head h reads kv head h // (n_heads / n_kv_heads): repeating each
+    # kv head's k and v projection rows for its group of query heads gives a
+    # block with n_kv_heads = n_heads that computes the same thing.
+    gqa = synth.Workload("gqa_rep", 256, 8, 2, 64, 512, rope_axes=(16, 24, 24), grid_h=8,
+                         grid_w=8, n_txt=8)
+    mha = dataclasses.replace(gqa, name="mha_rep", n_kv_heads=8)
+    nh, nkv, d = 8, 2, 64
+    w = synth.block_weights(gqa, 0, seed=0)
+    q, k, v = w["w_qkv"].split([nh * d, nkv * d, nkv * d])
+
+    def rep(t):
+        return t.reshape(nkv, d, -1).repeat_interleave(nh // nkv, dim=0).reshape(nh * d, -1)
+
+    w_mha = dict(w)
+    w_mha["w_qkv"] = torch.cat([q, rep(k), rep(v)]).contiguous()
+    x = synth.residual_input(gqa, seed=1)
+    mod = synth.modulation_input(gqa, seed=1)
+    got_gqa = run_block_gpu(gqa, w, x, mod) - npf(x)
+    got_mha = run_block_gpu(mha, w_mha, x, mod) - npf(x)
+    assert_block_parity(got_gqa, got_mha, frac=1e-3, what="GQA vs repeated MHA")
+
+
+def test_block_equals_its_stages():
+    # dit_block_forward enqueues the same kernels as its stage entry points:
+    # norm, QKV with qk-norm and RoPE, attention, gated out projection, norm,
+    # SwiGLU, gated down projection.  Same inputs, same order: bit-identical.
+    wl = SMALL_BLOCKS["gqa_small"]
+    n, H, F, d = wl.n_tokens, wl.hidden, wl.ffn, wl.head_dim
+    w = synth.block_weights(wl, 0, seed=0)
+    x = synth.residual_input(wl, seed=1)
+    mod = synth.modulation_input(wl, seed=1).to(dev()).contiguous()
+    cfg = dit.block_config_from(wl)
+    blk = dit.DeviceBlock(w, dev())
+    rc, rs = rope_tables(wl)
+    xb = x.to(dev()).contiguous()
+    dit.dit_block_forward(cfg, blk, xb, mod, rc, rs)
+    xs = x.to(dev()).contiguous()
+    a = torch.empty(n, H, dtype=torch.bfloat16, device=dev())
+    qk = torch.empty(wl.n_heads + wl.n_kv_heads, n, d, dtype=torch.bfloat16, device=dev())
+    vt = torch.empty(1, wl.n_kv_heads, d, (n + 7) // 8 * 8, dtype=torch.bfloat16, device=dev())
+    o = torch.empty(n, wl.n_heads * d, dtype=torch.bfloat16, device=dev())
+    h = torch.empty(n, F, dtype=torch.bfloat16, device=dev())
+    dit.dit_ln_modulate(0, xs, mod[0], mod[1], 1e-6, a)
+    dit.dit_qkv_rope(cfg, blk, a, rc, rs, qk, vt)
+    dit.dit_attention(cfg, qk, vt, o)
+    dit.dit_linear(dit.DIT_EPI_RESIDUAL, o, blk.t["w_o"], xs, mod[2])
+    dit.dit_ln_modulate(0, xs, mod[3], mod[4], 1e-6, a)
+    dit.dit_linear(dit.DIT_EPI_SWIGLU, a, blk.t["w_gu"], h)
+    dit.dit_linear(dit.DIT_EPI_RESIDUAL, h, blk.t["w_down"], xs, mod[5])
+    torch.cuda.synchronize()
+    assert dit.dit_last_device_error() == dit.DIT_OK
+    np.testing.assert_array_equal(npf(xs), npf(xb))
 
 
 def sample_rows(n):
