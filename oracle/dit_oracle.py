@@ -47,12 +47,36 @@ pin tests check.
 from __future__ import annotations
 
 import math
+import os
+from concurrent.futures import ThreadPoolExecutor
 from dataclasses import dataclass, field
-from typing import Optional, Sequence
+from typing import Callable, Optional, Sequence
 
 import numpy as np
 
 F32 = np.float32
+
+
+def _map(fn: Callable, items: Sequence) -> list:
+    """[fn(i) for i in items] on a thread pool over the host's cores.  Used
+    only for pieces of work that are independent by definition (one attention
+    head of one sequence; one chunk of rows of a row-wise coding): each piece
+    computes exactly what the serial loop computes, numpy releases the
+    interpreter lock inside its kernels, and the pool exists only for the
+    duration of the call."""
+    items = list(items)
+    n = min(len(items), os.cpu_count() or 1)
+    if n <= 1:
+        return [fn(i) for i in items]
+    with ThreadPoolExecutor(n) as ex:
+        return list(ex.map(fn, items))
+
+
+def _row_chunks(n_rows: int) -> list:
+    """Row ranges that split n_rows into about four pieces per host core."""
+    parts = max(1, min(n_rows, 4 * (os.cpu_count() or 1)))
+    step = -(-n_rows // parts)
+    return [(r, min(r + step, n_rows)) for r in range(0, n_rows, step)]
 
 
 # --------------------------------------------------------------------------
@@ -184,8 +208,12 @@ def quantize_rows_e4m3(y: np.ndarray):
 
 def rotate_quantize(x: np.ndarray):
     """Rotation then per-row coding of one operand: quantize_rows_e4m3 of
-    fwht256_rows(x)."""
-    return quantize_rows_e4m3(fwht256_rows(x))
+    fwht256_rows(x).  Both steps work on each row alone, so chunks of rows
+    are coded independently and stacked."""
+    x = x.astype(F32, copy=False)
+    parts = _map(lambda r: quantize_rows_e4m3(fwht256_rows(x[r[0]:r[1]])), _row_chunks(x.shape[0]))
+    return (np.concatenate([p[0] for p in parts], axis=0),
+            np.concatenate([p[1] for p in parts], axis=0))
 
 
 def linear_w8a8_h256(x: np.ndarray, w: np.ndarray) -> np.ndarray:
@@ -383,15 +411,18 @@ def attention(q: np.ndarray, k: np.ndarray, v: np.ndarray, n_heads: int,
     group = n_heads // n_kv_heads
     scale = F32(1.0 / math.sqrt(d))
     out = np.empty((n, n_heads, d), dtype=F32)
-    for s in range(n_seqs):
+
+    def one_head(sh):  # sequence s, query head h (independent of the others)
+        s, h = sh
         rows = slice(s * s_len, (s + 1) * s_len)
-        for h in range(n_heads):
-            g = h // group
-            sc = np.matmul(q[rows, h, :], k[rows, g, :].T).astype(F32) * scale
-            sc = sc - sc.max(axis=1, keepdims=True)
-            p = np.exp(sc).astype(F32)
-            p = p / p.sum(axis=1, keepdims=True, dtype=F32)
-            out[rows, h, :] = np.matmul(p, v[rows, g, :])
+        g = h // group
+        sc = np.matmul(q[rows, h, :], k[rows, g, :].T).astype(F32) * scale
+        sc = sc - sc.max(axis=1, keepdims=True)
+        p = np.exp(sc).astype(F32)
+        p = p / p.sum(axis=1, keepdims=True, dtype=F32)
+        out[rows, h, :] = np.matmul(p, v[rows, g, :])
+
+    _map(one_head, [(s, h) for s in range(n_seqs) for h in range(n_heads)])
     return out.reshape(n, n_heads * d)
 
 
@@ -405,13 +436,16 @@ def attention_rows(q_rows: np.ndarray, k: np.ndarray, v: np.ndarray, n_heads: in
     group = n_heads // n_kv_heads
     scale = F32(1.0 / math.sqrt(d))
     out = np.empty((r, n_heads, d), dtype=F32)
-    for h in range(n_heads):
+
+    def one_head(h):
         g = h // group
         sc = np.matmul(q_rows[:, h, :], k[:, g, :].T).astype(F32) * scale
         sc = sc - sc.max(axis=1, keepdims=True)
         p = np.exp(sc).astype(F32)
         p = p / p.sum(axis=1, keepdims=True, dtype=F32)
         out[:, h, :] = np.matmul(p, v[:, g, :])
+
+    _map(one_head, range(n_heads))
     return out.reshape(r, n_heads * d)
 
 

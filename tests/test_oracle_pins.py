@@ -570,3 +570,184 @@ def test_ernie_variant_block_invariants():
     np.testing.assert_allclose(a, b, rtol=1e-4, atol=1e-4)
     rows = np.array([2, 0, 9])
     np.testing.assert_allclose(O.block_forward_rows(cfg, w, x, mod, ang, rows), a[rows], rtol=1e-5, atol=1e-5)
+
+
+# ---------------------------------------------------------------- conditioning
+def _silu64(x):
+    return x / (1.0 + math.exp(-x))
+
+
+def _cond_weights(h, t_dim, sel, a, c, bm, b1=None, b2=None):
+    """Hand-built time MLP and modulation heads whose outputs have closed
+    forms: W1 row i picks sinusoid entry sel[i] times a[i]; W2 is diagonal
+    c; modulation row (chunk k, column i) picks temb[i] times (k + 1), bias
+    bm; the final head row (chunk k, column i) picks temb[i] times -(k + 1)."""
+    w1 = np.zeros((h, t_dim), F32)
+    for i, j in enumerate(sel):
+        w1[i, j] = a[i]
+    w2 = np.diag(np.asarray(c, F32))
+    mw = np.zeros((6 * h, h), F32)
+    fw = np.zeros((2 * h, h), F32)
+    for k in range(6):
+        for i in range(h):
+            mw[k * h + i, i] = k + 1
+    for k in range(2):
+        for i in range(h):
+            fw[k * h + i, i] = -(k + 1)
+    return {"t_w1": w1, "t_b1": np.zeros(h, F32) if b1 is None else b1,
+            "t_w2": w2, "t_b2": np.zeros(h, F32) if b2 is None else b2,
+            "mod_w": mw, "mod_b": bm, "fin_w": fw, "fin_b": np.zeros(2 * h, F32)}
+
+
+def test_conditioning_closed_form():
+    # [ERNIE] section IV: the six adaLN chunks [shift1, scale1, gate1, shift2,
+    # scale2, gate2] come from one H -> 6H linear of SiLU(temb), chunk k being
+    # output rows [kH, (k+1)H); temb = W2 SiLU(W1 e + b1) + b2 with e the
+    # sinusoid of T = 1000 sigma ([ZFLOW] section IV).  With one-hot weights
+    # every output has a closed form: at sigma = 0.5, T = 500 and the
+    # sinusoid entries 0 and 4 (t_dim 8, half 4: w_0 = 1) are cos 500 and
+    # sin 500.  A missing SiLU (either one), T = sigma, a transposed [6H]
+    # reshape or a swapped W1/W2 each changes some entry.
+    h, td = 4, 8
+    sel = [0, 4, 1, 5]                       # cos(T), sin(T), cos(T w_1), sin(T w_1)
+    a = [2.0, -3.0, 1.5, 0.5]
+    c = [1.0, 0.5, -2.0, 3.0]
+    b1 = np.array([0.25, -0.5, 0.0, 1.0], F32)
+    b2 = np.array([-0.75, 0.5, 0.125, 0.0], F32)
+    bm = np.arange(6 * h, dtype=F32) * F32(0.01)
+    mw = _cond_weights(h, td, sel, a, c, bm, b1, b2)
+    sigma = 0.5
+    mod, fin = O.conditioning(mw, sigma, td, 1000.0)
+    assert mod.shape == (6, h) and fin.shape == (2, h)
+    T = 1000.0 * sigma
+    w1 = 10000.0 ** (-1 / 4)
+    e = {0: math.cos(T), 4: math.sin(T), 1: math.cos(T * w1), 5: math.sin(T * w1)}
+    temb = [c[i] * _silu64(a[i] * e[sel[i]] + float(b1[i])) + float(b2[i]) for i in range(h)]
+    st = [_silu64(t) for t in temb]
+    for k in range(6):
+        for i in range(h):
+            want = (k + 1) * st[i] + float(bm[k * h + i])
+            assert abs(mod[k, i] - want) <= 2e-5 * (1 + abs(want)), (k, i, mod[k, i], want)
+    for k in range(2):
+        for i in range(h):
+            want = -(k + 1) * st[i]
+            assert abs(fin[k, i] - want) <= 2e-5 * (1 + abs(want)), (k, i, fin[k, i], want)
+
+
+def test_conditioning_sigma_zero_feeds_cos_ones():
+    # sigma = 0 gives T = 0 and the sinusoid [1 ... 1, 0 ... 0] (cosine half
+    # first): a W1 row summing the cosine half sees t_dim / 2, a row summing
+    # the sine half sees 0, whatever t_scale is.
+    h, td = 2, 16
+    mw = _cond_weights(h, td, [0, 0], [0.0, 0.0], [1.0, 1.0], np.zeros(6 * h, F32))
+    mw["t_w1"] = np.zeros((h, td), F32)
+    mw["t_w1"][0, : td // 2] = 0.25
+    mw["t_w1"][1, td // 2:] = 1.0
+    mod, _ = O.conditioning(mw, 0.0, td, 1000.0)
+    temb = [_silu64(0.25 * td / 2), _silu64(0.0)]
+    for i in range(h):
+        assert abs(mod[0, i] - _silu64(temb[i])) <= 1e-6
+
+
+# ---------------------------------------------------------------- step composition
+def _step_model(cfg, seed=4, n_layers=2, c_lat=8, td=16, gates_off=False):
+    r = np.random.default_rng(seed)
+    h = cfg.hidden
+    mw = {
+        "patch_w": r.standard_normal((h, c_lat)).astype(F32) * 0.3,
+        "patch_b": r.standard_normal(h).astype(F32) * 0.1,
+        "t_w1": r.standard_normal((h, td)).astype(F32) * 0.1, "t_b1": np.zeros(h, F32),
+        "t_w2": r.standard_normal((h, h)).astype(F32) * 0.1, "t_b2": np.zeros(h, F32),
+        "mod_w": r.standard_normal((6 * h, h)).astype(F32) * 0.3,
+        "mod_b": r.standard_normal(6 * h).astype(F32) * 0.3,
+        "fin_w": r.standard_normal((2 * h, h)).astype(F32) * 0.3,
+        "fin_b": r.standard_normal(2 * h).astype(F32) * 0.3,
+        "out_w": r.standard_normal((c_lat, h)).astype(F32) * 0.3,
+        "out_b": r.standard_normal(c_lat).astype(F32) * 0.1,
+        "layers": [tiny_weights(cfg, s) for s in range(n_layers)],
+    }
+    if gates_off:  # gate1 = gate2 = 0: chunks 2 and 5 of the modulation
+        for k in (2, 5):
+            mw["mod_w"][k * h:(k + 1) * h] = 0.0
+            mw["mod_b"][k * h:(k + 1) * h] = 0.0
+    mc = O.ModelConfig(block=cfg, n_layers=n_layers, latent_channels=c_lat, t_dim=td,
+                       rope_axes=AXES)
+    return mc, mw
+
+
+def test_denoise_step_zero_gates_is_head_then_tail():
+    # With both gates zero every block is the identity ([ERNIE] section IV,
+    # gated residuals), so the velocity is the final layer applied to the
+    # patch embedding of the latent: the image rows of the joint sequence are
+    # the patch-embedded latent, and the final layer reads those rows only
+    # (the text must not matter).  Reading the text rows, or putting the text
+    # first, fails this.
+    cfg = tiny_cfg()
+    mc, mw = _step_model(cfg, gates_off=True)
+    r = np.random.default_rng(9)
+    lat = r.standard_normal((12, 8)).astype(F32)
+    txt = r.standard_normal((3, cfg.hidden)).astype(F32)
+    _, v = O.denoise_step(mc, mw, lat, txt, 3, 4, 0.8, 0.7, return_velocity=True)
+    _, fin = O.conditioning(mw, 0.8, mc.t_dim, mc.t_scale)
+    want = O.final_layer(O.linear(lat, mw["patch_w"], mw["patch_b"]), fin, mw["out_w"],
+                         mw["out_b"], cfg.ln_eps)
+    np.testing.assert_allclose(v, want, rtol=1e-5, atol=1e-5)
+    _, v2 = O.denoise_step(mc, mw, lat, 5 * txt + 1, 3, 4, 0.8, 0.7, return_velocity=True)
+    np.testing.assert_array_equal(v2, v)
+
+
+def test_denoise_step_final_scale_minus_one_gives_shift_rows():
+    # fin = [scale, shift] ([ERNIE] section V, Bug 4): a final head whose
+    # weight is zero and whose bias is [-1 ... -1, s] makes every normed image
+    # row s, so every velocity row is s Wout^T + bout, whatever the latent,
+    # the text and the layers do.  A swapped chunk order fails.
+    cfg = tiny_cfg()
+    mc, mw = _step_model(cfg)
+    h = cfg.hidden
+    s = np.random.default_rng(3).standard_normal(h).astype(F32)
+    mw["fin_w"][:] = 0.0
+    mw["fin_b"] = np.concatenate([-np.ones(h, F32), s])
+    r = np.random.default_rng(10)
+    lat = r.standard_normal((12, 8)).astype(F32)
+    txt = r.standard_normal((3, h)).astype(F32)
+    _, v = O.denoise_step(mc, mw, lat, txt, 3, 4, 0.6, 0.5, return_velocity=True)
+    want = np.repeat((s @ mw["out_w"].T + mw["out_b"])[None], 12, axis=0)
+    np.testing.assert_allclose(v, want, rtol=1e-5, atol=1e-5)
+
+
+def test_denoise_step_text_reaches_image_rows_through_attention():
+    # With the gates on, the text rows take part in the joint attention, so
+    # changing the text changes the velocity of the image rows; and the
+    # velocity depends on sigma through the modulation (T = 1000 sigma).
+    cfg = tiny_cfg()
+    mc, mw = _step_model(cfg)
+    r = np.random.default_rng(11)
+    lat = r.standard_normal((12, 8)).astype(F32)
+    txt = r.standard_normal((3, cfg.hidden)).astype(F32)
+    _, v = O.denoise_step(mc, mw, lat, txt, 3, 4, 0.8, 0.7, return_velocity=True)
+    _, v_txt = O.denoise_step(mc, mw, lat, txt[::-1].copy(), 3, 4, 0.8, 0.7,
+                              return_velocity=True)
+    _, v_sig = O.denoise_step(mc, mw, lat, txt, 3, 4, 0.3, 0.2, return_velocity=True)
+    assert np.abs(v_txt - v).max() > 1e-3
+    assert np.abs(v_sig - v).max() > 1e-3
+
+
+def test_denoise_step_equals_its_stages():
+    # The step is its stages in the pages' order: conditioning at sigma,
+    # patch embedding of the latent, [image rows; text rows], positions
+    # (n_txt, h, w) / (j, 0, 0), the layers, the final layer on the image
+    # rows, the Euler update ([ERNIE] section IV; [ZFLOW] section IV).
+    cfg = tiny_cfg()
+    mc, mw = _step_model(cfg)
+    r = np.random.default_rng(12)
+    lat = r.standard_normal((12, 8)).astype(F32)
+    txt = r.standard_normal((3, cfg.hidden)).astype(F32)
+    new, v = O.denoise_step(mc, mw, lat, txt, 3, 4, 0.8, 0.7, return_velocity=True)
+    mod, fin = O.conditioning(mw, 0.8, mc.t_dim, mc.t_scale)
+    x = np.concatenate([O.linear(lat, mw["patch_w"], mw["patch_b"]), txt])
+    ang = O.rope_angles_3d(O.position_ids(3, 4, 3), AXES, 256.0)
+    for lw in mw["layers"]:
+        x = O.block_forward(cfg, lw, x, mod, ang)
+    want_v = O.final_layer(x[:12], fin, mw["out_w"], mw["out_b"], cfg.ln_eps)
+    np.testing.assert_array_equal(v, want_v)
+    np.testing.assert_array_equal(new, O.euler_step(lat, want_v, 0.8, 0.7))
