@@ -12,6 +12,7 @@ and make attention degenerate).
 """
 from __future__ import annotations
 
+import os
 import zlib
 from dataclasses import dataclass, field
 from typing import Dict, List, Sequence
@@ -150,8 +151,19 @@ def model_weights(wl: Workload, seed: int = 0, device="cpu", std: float = 0.02,
         "out_w": bf16(normal((c, h), "out_w", seed, std, device=device)),
         "out_b": bf16_valued(normal((c,), "out_b", seed, std, device=device)),
     }
-    w["layers"] = [block_weights(wl, li, seed, device, std) for li in range(nl)]
+    w["layers"] = _layers(wl, nl, seed, device, std)
     return w
+
+
+def _layers(wl: Workload, n_layers: int, seed: int, device, std: float) -> List[Dict]:
+    """Every layer's weights.  On the host the layers are drawn on a thread
+    pool (each tensor has its own generator, so the values do not depend on
+    the order or the thread they are drawn in)."""
+    if torch.device(device).type != "cpu" or n_layers <= 1:
+        return [block_weights(wl, li, seed, device, std) for li in range(n_layers)]
+    from concurrent.futures import ThreadPoolExecutor
+    with ThreadPoolExecutor(min(n_layers, os.cpu_count() or 1)) as ex:
+        return list(ex.map(lambda li: block_weights(wl, li, seed, device, std), range(n_layers)))
 
 
 def residual_input(wl: Workload, seed: int = 1, device="cpu") -> torch.Tensor:

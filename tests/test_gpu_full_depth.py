@@ -1,0 +1,150 @@
+"""Full-depth parity on the GPU against the oracle.
+
+The whole-step criterion of the workload: velocity cosine >= 0.999 after a
+full-depth flow-matching denoise step ("Porting ERNIE-Image-Turbo to Zig and
+Metal", section IV: 36 layers per step), for the 36-layer ERNIE-shaped
+denoiser and the 28-layer Krea-shaped GQA denoiser; the ERNIE-shaped step with
+its projections in the W8A8 format ("From Python + CUDA to Pure Rust + Metal
+4", section VII); and the 24-layer pre-norm ViT backbone (the makepad commit
+log for libs/ai/metal/shaders/ggml) compared on every row.
+
+The oracle evaluates every layer on every row in fp32 (minutes of host time
+for the ERNIE shape); the weights are drawn once per shape and shared by the
+tests of that shape."""
+import dataclasses
+import functools
+
+import numpy as np
+import pytest
+import torch
+
+from diffusion_transformer_image_gb300 import synth
+from gpu_common import (assert_block_parity, cosine, dev, max_err_vs_rms, npf, oracle_angles,
+                        oracle_block_config, oracle_weights)
+from oracle import dit_oracle as O
+
+pytestmark = pytest.mark.gpu
+
+dit = pytest.importorskip("diffusion_transformer_image_gb300.dit")
+
+SIGMAS = O.flowmatch_sigmas(8, 4.0)
+_REF = {}   # oracle velocities already computed, by (workload, format, step)
+
+
+@functools.lru_cache(maxsize=1)
+def model_weights(name):
+    """The seeded weights of a whole denoiser, drawn once per shape (host
+    bf16: 15.7 GB for the ERNIE shape, 21.8 GB for the Krea shape)."""
+    wl = synth.WORKLOADS[name]
+    return synth.model_weights(wl, seed=0, n_layers=wl.n_layers)
+
+
+class _LazyLayers:
+    """Per-layer oracle weights converted to fp32 on access, so a whole
+    model never sits in host memory in fp32 at once."""
+
+    def __init__(self, layers):
+        self.layers = layers
+
+    def __len__(self):
+        return len(self.layers)
+
+    def __getitem__(self, i):
+        return oracle_weights(self.layers[i])
+
+
+def oracle_step(wl, mw, step):
+    key = (wl.name, wl.linear_format, step)
+    if key not in _REF:
+        mc = O.ModelConfig(block=oracle_block_config(wl), n_layers=wl.n_layers,
+                           latent_channels=wl.latent_channels, t_dim=wl.t_dim,
+                           rope_axes=wl.rope_axes, rope_theta=wl.rope_theta)
+        ow = {k: synth.to_numpy_f32(v) for k, v in mw.items() if k != "layers"}
+        ow["layers"] = _LazyLayers(mw["layers"])
+        _REF[key] = O.denoise_step(mc, ow, npf(synth.latent_input(wl, seed=1)),
+                                   npf(synth.text_input(wl, seed=1)), wl.grid_h, wl.grid_w,
+                                   float(SIGMAS[step]), float(SIGMAS[step + 1]),
+                                   return_velocity=True)
+    return _REF[key]
+
+
+def gpu_step(wl, mw, step):
+    cfg = dit.model_config_from(wl)
+    model = dit.DeviceModel(mw, dev(), linear_format=wl.linear_format)
+    lat = synth.latent_input(wl, seed=1).to(dev()).contiguous()
+    v = torch.empty_like(lat)
+    dit.dit_denoise_step(cfg, model, lat, synth.text_input(wl, seed=1).to(dev()), wl.grid_h,
+                         wl.grid_w, float(SIGMAS[step]), float(SIGMAS[step + 1]), velocity_out=v)
+    torch.cuda.synchronize()
+    assert dit.dit_last_device_error() == dit.DIT_OK
+    out = npf(lat), npf(v)
+    del model
+    torch.cuda.empty_cache()
+    return out
+
+
+@pytest.mark.parametrize("name", ["ernie_full", "krea_gqa"])
+def test_denoise_step_full_depth(name):
+    """Velocity cosine >= 0.999 after a full-depth step at the first sigma of
+    the shift-4 schedule (36 ERNIE-shaped layers, 28 Krea-shaped layers)."""
+    wl = synth.WORKLOADS[name]
+    mw = model_weights(name)
+    lat, v = gpu_step(wl, mw, 0)
+    new_ref, v_ref = oracle_step(wl, mw, 0)
+    c = cosine(v, v_ref)
+    e, rms = max_err_vs_rms(v, v_ref)
+    print(f"{name}: {wl.n_layers} layers, velocity cosine {c:.6f}, max|err| {e / rms:.4f} x RMS, "
+          f"latent cosine {cosine(lat, new_ref):.6f}")
+    assert c >= 0.999
+    assert cosine(lat, new_ref) >= 0.999
+
+
+def test_denoise_step_full_depth_w8a8():
+    """The 36-layer ERNIE-shaped step with the four projections of every
+    block in the W8A8 format (256-point Hadamard rotation, e4m3 codes, fp32
+    row scales) against the oracle's W8A8 step: velocity cosine >= 0.999, and
+    the GPU velocity is closer to the oracle's W8A8 velocity than the
+    oracle's own bf16 velocity is (so the format, not only the model, is
+    reproduced)."""
+    base = synth.WORKLOADS["ernie_full"]
+    wl = dataclasses.replace(base, linear_format="w8a8_h256")
+    mw = model_weights(base.name)
+    lat, v = gpu_step(wl, mw, 0)
+    new_ref, v_ref = oracle_step(wl, mw, 0)
+    _, v_bf16 = oracle_step(base, mw, 0)
+    c = cosine(v, v_ref)
+    d_gpu = float(np.sqrt(np.mean((v.astype(np.float64) - v_ref) ** 2)))
+    d_fmt = float(np.sqrt(np.mean((v_bf16.astype(np.float64) - v_ref) ** 2)))
+    print(f"ernie_full W8A8: velocity cosine {c:.6f} (bf16 oracle vs W8A8 oracle "
+          f"{cosine(v_bf16, v_ref):.6f}); RMS distance GPU {d_gpu:.4e}, format {d_fmt:.4e}")
+    assert c >= 0.999
+    assert d_gpu < d_fmt
+    assert cosine(lat, new_ref) >= 0.999
+
+
+def test_vit_backbone_24_layers():
+    """The 24-layer pre-norm ViT backbone, 4 images x (5 + 32 x 32) tokens,
+    each image attending only to its own tokens, every layer through
+    dit_block_forward, against the oracle's vit_forward on every row."""
+    wl = synth.WORKLOADS["vit_backbone"]
+    layers = [synth.block_weights(wl, li, seed=0) for li in range(wl.n_layers)]
+    x = synth.residual_input(wl, seed=1)
+    cfg = dit.block_config_from(wl)
+    blocks = [dit.DeviceBlock(w, dev()) for w in layers]
+    half = wl.head_dim // 2
+    rc = torch.empty(wl.seq_len, half, device=dev())
+    rs = torch.empty_like(rc)
+    dit.dit_rope_table_vit(wl.grid_h, wl.grid_w, wl.n_prefix, wl.head_dim, 10000.0, rc, rs)
+    ws = dit.workspace(dit.dit_block_workspace_bytes(cfg, wl.n_tokens, wl.n_seqs), dev())
+    xg = x.to(dev()).contiguous()
+    for b in blocks:
+        dit.dit_block_forward(cfg, b, xg, None, rc, rs, n_seqs=wl.n_seqs, ws=ws)
+    torch.cuda.synchronize()
+    assert dit.dit_last_device_error() == dit.DIT_OK
+    got = npf(xg)
+    ref = O.vit_forward(oracle_block_config(wl), [oracle_weights(w) for w in layers], npf(x),
+                        oracle_angles(wl), wl.n_seqs)
+    e, rms = max_err_vs_rms(got, ref)
+    print(f"vit_backbone: 24 layers, cosine {cosine(got, ref):.6f}, max|err| {e / rms:.4f} x RMS")
+    assert cosine(got, ref) >= 0.999
+    assert_block_parity(got, ref, what="24-layer ViT")
