@@ -337,6 +337,8 @@ dit_status check_model(const dit_model_config* m) {
   if (m->n_layers < 0 || m->latent_channels <= 0 || m->t_dim <= 0 || m->t_dim % 8 != 0)
     return DIT_EINVAL;
   if (m->latent_channels % 8 != 0) return DIT_EUNSUPPORTED;
+  // the time MLP's first linear stages the whole sinusoid in shared memory
+  if (m->t_dim > GEMV_MAX_K) return DIT_EUNSUPPORTED;
   const int half = m->block.head_dim / 2;
   if (m->rope_axes[0] % 2 || m->rope_axes[1] % 2 || m->rope_axes[2] % 2 ||
       (m->rope_axes[0] + m->rope_axes[1] + m->rope_axes[2]) / 2 != half)

@@ -104,6 +104,8 @@ cudaError_t launch_ln_rotate_quant(int mode, const float* x, long long ldx, int 
                                    const float* p0, const float* p1, float eps, uint8_t* q,
                                    long long ldq, float* scale, cudaStream_t st);
 cudaError_t launch_euler(float* x, const float* v, long long n, float dt, cudaStream_t st);
+// Longest input vector of the M = 1 linears (staged whole in shared memory).
+constexpr int GEMV_MAX_K = 16384;
 cudaError_t launch_gemv(const __nv_bfloat16* W, const float* x, const float* b, float* y,
                         int O, int K, int silu_in, cudaStream_t st);
 cudaError_t launch_sinusoid(float T, int dim, float* out, cudaStream_t st);

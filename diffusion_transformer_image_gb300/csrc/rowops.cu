@@ -348,7 +348,7 @@ cudaError_t launch_euler(float* x, const float* v, long long n, float dt, cudaSt
 
 cudaError_t launch_gemv(const __nv_bfloat16* W, const float* x, const float* b, float* y, int O,
                         int K, int silu_in, cudaStream_t st) {
-  if ((K & 7) || K > 16384) return cudaErrorInvalidValue;
+  if ((K & 7) || K > GEMV_MAX_K) return cudaErrorInvalidValue;
   const int rows_per_block = 8 * GEMV_ROWS_PER_WARP;
   const int grid = (O + rows_per_block - 1) / rows_per_block;
   const size_t smem = (size_t)K * sizeof(float);
@@ -358,7 +358,7 @@ cudaError_t launch_gemv(const __nv_bfloat16* W, const float* x, const float* b, 
     cudaGetDevice(&dev);
     if (dev < 64 && !attr_set[dev]) {
       cudaError_t e = cudaFuncSetAttribute(gemv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           16384 * (int)sizeof(float));
+                                           GEMV_MAX_K * (int)sizeof(float));
       if (e != cudaSuccess) return e;
       attr_set[dev] = true;
     }

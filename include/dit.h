@@ -114,7 +114,7 @@ typedef struct {
   dit_block_config block;
   int32_t n_layers;
   int32_t latent_channels;  /* C (128) */
-  int32_t t_dim;            /* sinusoid width (256) */
+  int32_t t_dim;            /* sinusoid width (256); a multiple of 8, <= 16384 */
   float t_scale;            /* timestep T = t_scale * sigma (1000) */
   int32_t rope_axes[3];     /* per-axis RoPE widths, sum = head_dim ([32,48,48]) */
   float rope_theta;         /* 256 */
@@ -321,6 +321,9 @@ dit_status dit_timestep_conditioning(const dit_model_config* cfg,
  *
  * Limits and behaviour:
  *   - t_dim + 2 * hidden > 32768 returns DIT_EUNSUPPORTED (nothing enqueued).
+ *     Within the model limits (t_dim <= 16384, hidden <= 8192) the scratch
+ *     always suffices; t_dim > 16384 returns DIT_EUNSUPPORTED, as it does
+ *     for every call that takes a dit_model_config.
  *   - Allocates nothing: no cudaMalloc, cudaFree or allocating library call.
  *   - The first call on a device asks the runtime for the array's device
  *     address (once per device, that device current); make that first call

@@ -170,3 +170,31 @@ def test_short_workspace_is_rejected_before_any_launch(dit):
                                    ctypes.c_void_p(fake), ctypes.c_void_p(fake),
                                    ctypes.c_void_p(fake), ctypes.c_void_p(fake + 8), need, None)
     assert st == dit.DIT_EINVAL
+
+
+def test_conditioning_t_dim_limit_rejected_before_any_launch(dit):
+    # The time MLP's first linear stages the sinusoid in shared memory, so
+    # t_dim is at most 16384: larger is DIT_EUNSUPPORTED from the host check,
+    # before the weights are even looked at (they are null here, which would
+    # otherwise be DIT_EINVAL) -- for the allocating and the allocation-free
+    # conditioning and for the step.  t_dim = 16392 with hidden 64 stays far
+    # inside the allocation-free entry point's static scratch (16392 + 128
+    # floats), so this is the t_dim limit and not the scratch limit.
+    from diffusion_transformer_image_gb300 import synth
+    for t_dim in (16392, 16400):
+        wl = synth.Workload("wide_t", hidden=64, n_heads=1, n_kv_heads=1, head_dim=64, ffn=128,
+                            rope_axes=(16, 8, 8), t_dim=t_dim)
+        cfg = dit.model_config_from(wl, 0)
+        w = ctypes.byref(dit.ModelWeights())
+        assert dit.lib.dit_timestep_conditioning_noalloc(ctypes.byref(cfg), w, 0.5, None, None,
+                                                         None) == dit.DIT_EUNSUPPORTED
+        assert dit.lib.dit_timestep_conditioning(ctypes.byref(cfg), w, 0.5, None, None, None,
+                                                 None) == dit.DIT_EUNSUPPORTED
+        assert dit.lib.dit_denoise_workspace_bytes(ctypes.byref(cfg), 8, 8, 0) == 0
+    # the largest accepted t_dim passes the shape checks and stops at the null weights
+    wl = synth.Workload("max_t", hidden=64, n_heads=1, n_kv_heads=1, head_dim=64, ffn=128,
+                        rope_axes=(16, 8, 8), t_dim=16384)
+    cfg = dit.model_config_from(wl, 0)
+    assert dit.lib.dit_timestep_conditioning_noalloc(
+        ctypes.byref(cfg), ctypes.byref(dit.ModelWeights()), 0.5, None, None,
+        None) == dit.DIT_EINVAL
