@@ -45,6 +45,20 @@ def test_krea_shaped_flops_use_the_kv_heads():
     assert sum(per_block.values()) == pytest.approx(1.039e12, rel=1e-3)
 
 
+def test_vit_flops_attend_within_each_image_and_have_no_head_tail():
+    # 4 images x 1029 tokens: attention is 4 x 1029^2 x 64 x 16 x 4, not
+    # (4 x 1029)^2; the pre-norm backbone has no patch embedding, time MLP or
+    # output projection in its count
+    wl = synth.WORKLOADS["vit_backbone"]
+    per_block, fwd = bench.workload_flops(wl, wl.n_layers)
+    n, S, H, d, nh, F = 4 * 1029, 1029, 1024, 64, 16, 4096
+    assert per_block["attention"] == 4 * (4 * S * S * d * nh)
+    assert per_block["qkv"] == 2 * n * H * 3 * nh * d
+    assert per_block["gate_up"] == 2 * n * H * 2 * F
+    assert fwd == 24 * sum(per_block.values())
+    assert sum(per_block.values()) == pytest.approx(1.55e11, rel=1e-2)
+
+
 # ------------------------------------------------------------ clock record
 class _FakeSmi:
     def __init__(self, out):
