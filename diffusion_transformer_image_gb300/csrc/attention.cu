@@ -12,16 +12,17 @@
 //   warp 0       TMA producer: both q tiles, then k tiles of 128 keys
 //   warp 2       TMA producer: v tiles (transposed, 128 keys)
 //   warp 1       TMEM allocator and MMA issuer, per key block j and tile t:
-//                  O_t += P_t(j) v_j  (P read from TMEM), then
+//                  O_t += P_t(j) v_j in two halves of 64 keys, each issued as
+//                  soon as the softmax has stored that half of P (P read
+//                  from TMEM), then
 //                  S_t(j+1) = q_t k_{j+1}^T into the columns P_t(j) occupies
 //                  (issue order is execution order on the tensor core).
-//   warps 3..18  softmax, eight per tile: query row r of tile t is shared by
-//                two warps (the same TMEM lane quarter), each owning 64 of
-//                the 128 scores of a block.  They exchange row maxima through
-//                shared memory (one barrier meeting per block), keep the
-//                running maximum and their partial
-//                sums, overwrite S_t with P_t (bf16, two per 32-bit column),
-//                and rescale their half of O_t when the maximum grows by more
+//   warps 3..10  softmax, four per tile, one per TMEM lane quarter: thread r
+//                owns query row r of its tile and all 128 scores of a block,
+//                so the row maximum needs no exchange between threads.  It
+//                keeps the running maximum and its row sum, overwrites S_t
+//                with P_t (bf16, two per 32-bit column) one half at a time,
+//                and rescales its row of O_t when the maximum grows by more
 //                than 2^8 (smaller growth is absorbed: exponentials stay
 //                <= 256).  While the softmax of one tile runs, the tensor
 //                core works on the other tile.
@@ -38,8 +39,8 @@ namespace dit {
 namespace {
 
 constexpr int BQ = 128, BKV = 128;
-constexpr int NUM_THREADS = 19 * 32;
-constexpr int NUM_SOFTMAX_WARPS = 16;   // 8 per query tile
+constexpr int NUM_SOFTMAX_WARPS = 8;    // 4 per query tile, one per TMEM lane quarter
+constexpr int NUM_THREADS = (3 + NUM_SOFTMAX_WARPS) * 32;
 constexpr float RESCALE_LOG2 = 8.0f;
 
 // Ring depths per head width, sized to 227 KB of shared memory.
@@ -65,11 +66,7 @@ struct AttnLayout {
   static constexpr int OFF_K = OFF_Q + 2 * Q_BYTES;
   static constexpr int OFF_V = OFF_K + KS * K_BYTES;
   static constexpr int OFF_BAR = OFF_V + VS * V_BYTES;
-  // Row-maximum exchange between the two softmax warps of a row:
-  // maxima [tile][block parity][half][row] fp32, final sums [tile][half][row].
-  static constexpr int OFF_RED = OFF_BAR + 512;
-  static constexpr int OFF_LSUM = OFF_RED + 2 * 2 * 2 * BQ * 4;
-  static constexpr int END = OFF_LSUM + 2 * 2 * BQ * 4;
+  static constexpr int END = OFF_BAR + 512;
   static constexpr int O_COL = 2 * BKV;           // O_A, then O_B
   static_assert(O_COL + 2 * HD <= 512, "TMEM overflow");
 };
@@ -79,8 +76,8 @@ constexpr int MAX_STAGES = 6;
 struct AttnBars {
   uint64_t q_full;
   uint64_t k_full[MAX_STAGES], k_empty[MAX_STAGES], v_full[MAX_STAGES], v_empty[MAX_STAGES];
-  uint64_t s_full[2], p_full[2], pv_done[2];   // per query tile
-  uint64_t xchg[2][4];  // per tile and TMEM lane quarter: the two warps of those rows
+  uint64_t s_full[2], pv_done[2];   // per query tile
+  uint64_t p_half[2][2];            // per query tile and half of P (64 keys)
   uint64_t drain;
   uint32_t tmem_slot;
 };
@@ -90,19 +87,6 @@ static_assert(sizeof(AttnBars) <= 512, "barrier block overflows its slot");
 template <int HD>
 constexpr size_t attn_smem_bytes() {
   return (size_t)AttnLayout<HD>::END + 1024;  // + slack to align the base to 1024 B
-}
-
-// The two softmax warps that share a tile's TMEM lane quarter meet here: each
-// arrives once (lane 0, after the warp's shared-memory writes), then waits for
-// the other.  Bounded like every other wait.
-__device__ __forceinline__ bool pair_sync(uint64_t* bar, uint32_t& uses, const DevErr& e) {
-  tc_fence_before();
-  __syncwarp();
-  if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
-  const bool ok = mbar_wait(bar, uses & 1u, e);
-  tc_fence_after();
-  ++uses;
-  return ok;
 }
 
 struct AttnParams {
@@ -124,13 +108,17 @@ __device__ __forceinline__ void issue_s(uint32_t s_tmem, uint32_t q_addr, uint32
   }
 }
 
+// O += P[:, 64 half : 64 half + 64] v[64 half : 64 half + 64, :]: four MMAs
+// of 16 keys; P half h sits in TMEM columns [32 h, 32 h + 32), v's keys
+// [64 h, 64 h + 64) in panel h of the stage.
 template <int HD>
-__device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem, uint32_t v_addr,
-                                         bool first) {
+__device__ __forceinline__ void issue_pv_half(uint32_t o_tmem, uint32_t p_tmem, uint32_t v_addr,
+                                              int half, bool first) {
   using L = AttnLayout<HD>;
   constexpr uint32_t idesc_o = idesc_bf16_f32(BQ, HD);
 #pragma unroll
-  for (int k = 0; k < BKV / 16; ++k) {
+  for (int kk = 0; kk < 4; ++kk) {
+    const int k = half * 4 + kk;
     const uint32_t voff = (k >> 2) * L::V_PANEL + (k & 3) * 32;
     umma_bf16_ts(o_tmem, p_tmem + k * 8, sdesc_sw128(v_addr + voff), idesc_o,
                  (!first || k > 0) ? 1u : 0u);
@@ -168,9 +156,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(&bars->s_full[t], 1);
-      mbar_init(&bars->p_full[t], NUM_SOFTMAX_WARPS / 2);
       mbar_init(&bars->pv_done[t], 1);
-      for (int q = 0; q < 4; ++q) mbar_init(&bars->xchg[t][q], 2);
+      for (int hf = 0; hf < 2; ++hf) mbar_init(&bars->p_half[t][hf], NUM_SOFTMAX_WARPS / 2);
     }
     mbar_init(&bars->drain, 1);
     fence_barrier_init();
@@ -249,10 +236,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         umma_commit(&bars->s_full[1]);
         umma_commit(&bars->k_empty[0]);
       }
-      // Per key block j, tile by tile: O_t += P_t(j) v_j, then S_t(j+1)
-      // (queued behind that PV).  Tile A's chain never waits on tile B's
-      // softmax, so the two softmax groups alternate on the special-function
-      // units while the tensor core works on the other tile.
+      // Per key block j, tile by tile: O_t += P_t(j) v_j half by half, then
+      // S_t(j+1) (queued behind that PV).  Tile A's chain never waits on tile
+      // B's softmax, so the two softmax groups alternate on the
+      // special-function units while the tensor core works on the other tile.
       for (int j = 0; j < nb && ok; ++j) {
         const int vs = j % L::VS;
         const uint32_t v_addr = smem_u32(smem + L::OFF_V + vs * L::V_BYTES);
@@ -260,13 +247,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const uint32_t k_addr = smem_u32(smem + L::OFF_K + st * L::K_BYTES);
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
-          if (!mbar_wait(&bars->p_full[t], j & 1, p.err) ||
-              (t == 0 && !mbar_wait(&bars->v_full[vs], (j / L::VS) & 1, p.err))) {
-            ok = false;
-            break;
+          const uint32_t o_t = tmem_base + L::O_COL + t * HD;
+          const uint32_t p_t = tmem_base + t * BKV;
+#pragma unroll
+          for (int hf = 0; hf < 2; ++hf) {
+            if (!mbar_wait(&bars->p_half[t][hf], j & 1, p.err) ||
+                (t == 0 && hf == 0 && !mbar_wait(&bars->v_full[vs], (j / L::VS) & 1, p.err))) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            issue_pv_half<HD>(o_t, p_t, v_addr, hf, j == 0);
           }
-          tc_fence_after();
-          issue_pv<HD>(tmem_base + L::O_COL + t * HD, tmem_base + t * BKV, v_addr, j == 0);
+          if (!ok) break;
           umma_commit(&bars->pv_done[t]);
           if (t == 1) umma_commit(&bars->v_empty[vs]);
           if (j + 1 < nb) {
@@ -289,20 +282,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
   } else {
     // ---------------------------------------------------- softmax warps
-    constexpr int HC = BKV / 2;  // score columns per thread
-    constexpr int OC = HD / 2;   // output columns per thread
-    const int idx = warp - 3;    // 0..15
-    const int t = idx >> 3;      // query tile
-    const int half = (idx >> 2) & 1;
-    const int quarter = warp & 3;  // TMEM lane quarter this warp may access
-    const int r = quarter * 32 + lane;  // query row within the tile
+    constexpr int OC = HD;       // output columns per thread (its whole row)
+    const int t = (warp - 3) >> 2;       // query tile
+    const int quarter = warp & 3;        // TMEM lane quarter this warp may access
+    const int r = quarter * 32 + lane;   // query row within the tile
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
     const uint32_t s_tmem = tmem_base + t * BKV + lane_off;
-    const uint32_t o_tmem = tmem_base + L::O_COL + t * HD + lane_off + half * OC;
-    uint64_t* xbar = &bars->xchg[t][quarter];
-    uint32_t xuses = 0;
-    float* red = reinterpret_cast<float*>(smem + L::OFF_RED) + t * 2 * 2 * BQ;
-    float* lsum = reinterpret_cast<float*>(smem + L::OFF_LSUM) + t * 2 * BQ;
+    const uint32_t o_tmem = tmem_base + L::O_COL + t * HD + lane_off;
     float m_used = -CUDART_INF_F;
     float l = 0.f;
     bool ok = true;
@@ -312,41 +298,30 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         break;
       }
       tc_fence_after();
-      float s[HC];
+      float s[BKV];
       __syncwarp();
-      tmem_ld64(s_tmem + half * HC, s);
+      tmem_ld128(s_tmem, s);
 
-      const int kv0 = ((j + kb0) % nb) * BKV + half * HC;
-      if (kv0 + HC > p.s_len) {
+      const int kv0 = ((j + kb0) % nb) * BKV;
+      if (kv0 + BKV > p.s_len) {
 #pragma unroll
-        for (int c = 0; c < HC; ++c)
+        for (int c = 0; c < BKV; ++c)
           if (kv0 + c >= p.s_len) s[c] = -CUDART_INF_F;
       }
-      // row maximum of this half: chain i takes s[i], s[i + 8], ..., s[i + 56]
-      // with three-input maxima
-      static_assert(HC == 64, "eight chains of eight scores");
-      float m8[8];
+      // row maximum: chain i takes s[i], s[i + 16], ..., s[i + 112] with
+      // three-input maxima
+      float m16[16];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        m8[i] = fmax3(s[i], s[i + 8], s[i + 16]);
-        m8[i] = fmax3(m8[i], s[i + 24], s[i + 32]);
-        m8[i] = fmax3(m8[i], s[i + 40], s[i + 48]);
-        m8[i] = fmaxf(m8[i], s[i + 56]);
+      for (int i = 0; i < 16; ++i) {
+        m16[i] = fmax3(s[i], s[i + 16], s[i + 32]);
+        m16[i] = fmax3(m16[i], s[i + 48], s[i + 64]);
+        m16[i] = fmax3(m16[i], s[i + 80], s[i + 96]);
+        m16[i] = fmaxf(m16[i], s[i + 112]);
       }
-      const float lmax = fmaxf(fmax3(m8[0], m8[1], m8[2]),
-                               fmax3(fmax3(m8[3], m8[4], m8[5]), m8[6], m8[7]));
-      // The exchange also orders the two halves' reads of S_t before either
-      // overwrites S_t's columns with P_t below.  Maxima alternate between
-      // two slots, so one meeting per block suffices: a slot is rewritten
-      // two blocks later, and the partner read it before its next arrival.
-      float* slot = red + (j & 1) * 2 * BQ;
-      slot[half * BQ + r] = lmax;
-      if (!pair_sync(xbar, xuses, p.err)) {
-        ok = false;
-        break;
-      }
-      const float omax = slot[(1 - half) * BQ + r];
-      const float mx = fmaxf(lmax, omax) * p.scale_log2;
+#pragma unroll
+      for (int i = 0; i < 5; ++i) m16[i] = fmax3(m16[i], m16[i + 5], m16[i + 10]);
+      const float mx =
+          fmaxf(fmax3(m16[0], m16[1], m16[2]), fmax3(m16[3], m16[4], m16[15])) * p.scale_log2;
 
       const bool need = mx > m_used + RESCALE_LOG2;
       if (__any_sync(0xffffffffu, need) && j > 0) {
@@ -366,39 +341,42 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       if (need) m_used = mx;
 
       // P_t(j) in bf16, two per 32-bit column, into the first half of S_t's
-      // columns: this half's 64 keys land in columns [32 half, 32 half + 32).
-      // exponent arguments and row sums two at a time (packed fp32: each lane
-      // rounds exactly like the scalar fmaf / add)
+      // columns, 64 keys at a time: keys [64 h, 64 h + 64) land in columns
+      // [32 h, 32 h + 32), and each half is handed to the MMA issuer as soon
+      // as it is stored.  Exponent arguments and row sums two at a time
+      // (packed fp32: each lane rounds exactly like the scalar fmaf / add).
       float2 r4[4] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};
       const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
       const float2 nm2 = make_float2(-m_used, -m_used);
 #pragma unroll
-      for (int ch = 0; ch < HC / 32; ++ch) {
-        uint32_t pk[16];
+      for (int hf = 0; hf < 2; ++hf) {
 #pragma unroll
-        for (int c = 0; c < 32; c += 2) {
-          const float2 x = __ffma2_rn(make_float2(s[ch * 32 + c], s[ch * 32 + c + 1]), sc2, nm2);
-          const float2 e = make_float2(ex2_approx(x.x), ex2_approx(x.y));
-          r4[(c >> 1) & 3] = __fadd2_rn(r4[(c >> 1) & 3], e);
-          pk[c / 2] = pack_bf16x2(e.x, e.y);
+        for (int ch = 0; ch < 2; ++ch) {
+          const int c0 = hf * 64 + ch * 32;
+          uint32_t pk[16];
+#pragma unroll
+          for (int c = 0; c < 32; c += 2) {
+            const float2 x = __ffma2_rn(make_float2(s[c0 + c], s[c0 + c + 1]), sc2, nm2);
+            const float2 e = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+            r4[(c >> 1) & 3] = __fadd2_rn(r4[(c >> 1) & 3], e);
+            pk[c / 2] = pack_bf16x2(e.x, e.y);
+          }
+          __syncwarp();
+          tmem_st16u_nowait(s_tmem + c0 / 2, pk);
         }
+        tmem_wait_st();   // this half of P is in TMEM before the MMA may read it
+        tc_fence_before();
         __syncwarp();
-        tmem_st16u_nowait(s_tmem + half * (HC / 2) + ch * 16, pk);
+        if (lane == 0) mbar_arrive(&bars->p_half[t][hf]);
       }
       l += ((r4[0].x + r4[0].y) + (r4[1].x + r4[1].y)) + ((r4[2].x + r4[2].y) + (r4[3].x + r4[3].y));
-      tmem_wait_st();  // both chunks of P are in TMEM before the MMA may read them
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->p_full[t]);
     }
     if (ok) {
       if (mbar_wait(&bars->pv_done[t], (nb - 1) & 1, p.err)) {
         tc_fence_after();
-        lsum[half * BQ + r] = l;
-        pair_sync(xbar, xuses, p.err);
-        const float inv_l = 1.0f / (l + lsum[(1 - half) * BQ + r]);
+        const float inv_l = 1.0f / l;
         const int row = q0 + t * BQ + r;
-        __nv_bfloat16* dst = p.o + ((size_t)seq * p.s_len + row) * p.ldo + h * HD + half * OC;
+        __nv_bfloat16* dst = p.o + ((size_t)seq * p.s_len + row) * p.ldo + h * HD;
         __syncwarp();
 #pragma unroll 1
         for (int c = 0; c < OC / 32; ++c) {
