@@ -207,6 +207,19 @@ __device__ __forceinline__ void scale_cols(float (&v)[32], float rs, const float
   }
 }
 
+// Output tile coordinates of tile t: groups of group_m row blocks, row blocks
+// fastest inside a group, so the pairs working at one time share the A rows
+// of their group (and B tiles) in L2.
+__device__ __forceinline__ void tile_coords(const GemmParams& p, int t, int& m_blk, int& n_blk) {
+  const int per_group = p.group_m * p.num_n;
+  const int g = t / per_group;
+  const int first = g * p.group_m;
+  const int rows = min(p.group_m, p.num_m - first);
+  const int idx = t - g * per_group;
+  m_blk = first + idx % rows;
+  n_blk = idx / rows;
+}
+
 // ---------------------------------------------------------------- epilogues
 // row: this thread's output row; row0: the first row of its warp's slab.
 template <int EPI, int HD, bool F8>
@@ -478,7 +491,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       uint32_t phase = 0, filled = 0, fill_parity = 0;
       bool ok = true;
       for (int t = pair; t < num_tiles && ok; t += num_pairs) {
-        const int m_blk = t % p.num_m, n_blk = t / p.num_m;
+        int m_blk, n_blk;
+        tile_coords(p, t, m_blk, n_blk);
         const int a_row = m_blk * PM + (int)rank * BM;
         // GLU tiles: rank 0 stages the 128 gate rows, rank 1 the matching up rows
         const int b_row = (EPI == EPI_SWIGLU || EPI == EPI_GEGLU)
@@ -564,7 +578,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const uint32_t te1 = mapa_shared(smem_u32(&bars->tempty[1]), 0);
     int local = 0;
     for (int t = pair; t < num_tiles; t += num_pairs, ++local) {
-      const int m_blk = t % p.num_m, n_blk = t / p.num_m;
+      int m_blk, n_blk;
+      tile_coords(p, t, m_blk, n_blk);
       const int acc = local & 1;
       const uint32_t acc_phase = (local >> 1) & 1;
       if (!mbar_wait(&bars->tfull[acc], acc_phase, p.err)) break;
@@ -667,6 +682,13 @@ cudaError_t launch_gemm_t(int epi, int hd, const void* A, long long lda, const v
   }
   p.num_m = (p.M + PM - 1) / PM;
   p.num_n = glu ? p.N / 128 : (p.N + BN - 1) / BN;
+  // raster groups of row blocks whose A rows take at most ~40 MB of L2
+  {
+    const long long a_bytes = (long long)PM * p.K * ES;
+    long long g = (40ll << 20) / (a_bytes > 0 ? a_bytes : 1);
+    if (g < 1) g = 1;
+    p.group_m = g < p.num_m ? (int)g : p.num_m;
+  }
   p.err = dev_err(ds);
   const int tiles = p.num_m * p.num_n;
   const int sms = ds->sm_count;

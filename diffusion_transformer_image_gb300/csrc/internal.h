@@ -69,6 +69,7 @@ struct GemmParams {
   float scalar;         // EPI_EULER: sigma_next - sigma
   QkvEpi qkv;
   DevErr err;
+  int group_m;          // row blocks per raster group (tiles walk rows fastest inside one)
 };
 
 // D = A[M,K] B[rows,K]^T with the epilogue `epi`; hd selects the QKV head
