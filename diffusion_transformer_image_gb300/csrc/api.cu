@@ -61,10 +61,63 @@ const DeviceState* device_state() {
 
 void count_launch(int n) { t_launches += n; }
 
+namespace {
+
+// Encoded tensor maps, cached per host thread and keyed by every argument of
+// the encode call (and the device): a hit returns exactly the map a fresh
+// encode would.  Direct-mapped on a hash of the key; a colliding key simply
+// replaces the entry.  Saves the host the ~500 encodes of a denoise step.
+struct TmapKey {
+  const void* base;
+  uint64_t dims[5];
+  uint64_t strides[4];
+  uint32_t box[5];
+  uint32_t elem_bytes;
+  int rank;
+  int dev;
+  int swizzle;
+};
+struct TmapEntry {
+  TmapKey key;
+  CUtensorMap map;
+  bool valid;
+};
+constexpr int TMAP_CACHE_SLOTS = 512;
+thread_local TmapEntry t_tmap_cache[TMAP_CACHE_SLOTS];
+
+uint64_t tmap_key_hash(const TmapKey& k) {
+  // FNV-1a over the key's bytes
+  const unsigned char* b = reinterpret_cast<const unsigned char*>(&k);
+  uint64_t h = 1469598103934665603ull;
+  for (size_t i = 0; i < sizeof(TmapKey); ++i) h = (h ^ b[i]) * 1099511628211ull;
+  return h;
+}
+
+}  // namespace
+
 bool make_tmap(CUtensorMap* map, uint32_t elem_bytes, const void* base, int rank,
-               const uint64_t* dims, const uint64_t* strides_bytes, const uint32_t* box) {
+               const uint64_t* dims, const uint64_t* strides_bytes, const uint32_t* box,
+               bool swizzle128) {
   if (g_encode == nullptr || !aligned16(base)) return false;
   if (elem_bytes != 1 && elem_bytes != 2 && elem_bytes != 4) return false;
+  if (rank < 1 || rank > 5) return false;
+  TmapKey key;
+  memset(&key, 0, sizeof(key));   // padding bytes take part in the hash and the compare
+  key.base = base;
+  key.elem_bytes = elem_bytes;
+  key.rank = rank;
+  key.swizzle = swizzle128 ? 1 : 0;
+  if (cudaGetDevice(&key.dev) != cudaSuccess) return false;
+  for (int i = 0; i < rank; ++i) {
+    key.dims[i] = dims[i];
+    key.box[i] = box[i];
+    if (i + 1 < rank) key.strides[i] = strides_bytes[i];
+  }
+  TmapEntry& slot = t_tmap_cache[tmap_key_hash(key) % TMAP_CACHE_SLOTS];
+  if (slot.valid && memcmp(&slot.key, &key, sizeof(key)) == 0) {
+    *map = slot.map;
+    return true;
+  }
   cuuint64_t gd[5];
   cuuint64_t gs[4];
   cuuint32_t bx[5];
@@ -84,9 +137,14 @@ bool make_tmap(CUtensorMap* map, uint32_t elem_bytes, const void* base, int rank
                                           : CU_TENSOR_MAP_DATA_TYPE_UINT8,
                         (cuuint32_t)rank,
                         const_cast<void*>(base), gd, gs, bx, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
+  if (r != CUDA_SUCCESS) return false;
+  slot.key = key;
+  slot.map = *map;
+  slot.valid = true;
+  return true;
 }
 
 namespace {

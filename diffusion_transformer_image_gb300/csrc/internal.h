@@ -21,11 +21,12 @@ const DeviceState* device_state();  // nullptr if CUDA is unusable
 inline DevErr dev_err(const DeviceState* ds) { return DevErr{ds->err, ds->timeout_ns}; }
 void count_launch(int n = 1);
 
-// Encodes a row-major tensor map with 128-byte swizzle: bf16 elements
-// (elem_bytes 2), fp32 (4) or bytes (1, the e4m3 codes).
+// Encodes a row-major tensor map with 128-byte swizzle (or none): bf16
+// elements (elem_bytes 2), fp32 (4) or bytes (1, the e4m3 codes).
 // dims[0] is the contiguous dimension; strides_bytes has rank-1 entries.
 bool make_tmap(CUtensorMap* map, uint32_t elem_bytes, const void* base, int rank,
-               const uint64_t* dims, const uint64_t* strides_bytes, const uint32_t* box);
+               const uint64_t* dims, const uint64_t* strides_bytes, const uint32_t* box,
+               bool swizzle128 = true);
 inline bool make_tmap_bf16(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
                            const uint64_t* strides_bytes, const uint32_t* box) {
   return make_tmap(map, 2, base, rank, dims, strides_bytes, box);
