@@ -15,20 +15,26 @@ namespace {
 // ([ERNIE] "Porting ERNIE-Image-Turbo to Zig and Metal", section IV and
 // section V, Bug 4; [ZFLOW] section VI `plus_one`: the 1 is added on the
 // device) or the affine `n g + b` of the pre-norm ViT ([MAKEPAD]).  One
-// 128-thread block per row, the row held in registers (H <= 128 * 4 * MAXV),
-// mean and variance by warp shuffles plus one shared-memory exchange.
-constexpr int LN_THREADS = 128;
-constexpr int LN_MAXV = 16;  // float4 per thread: H <= 8192 (8 for H <= 4096: fewer
-                             // registers, more rows in flight per SM)
+// 256-thread block per row, the row held in registers (H <= 256 * 4 * MAXV),
+// mean and variance by warp shuffles plus one shared-memory exchange.  A
+// 256-thread block keeps a thread's share of a 4096-wide row at four 16-byte
+// vectors, so more rows are in flight per SM and the last wave of rows is a
+// small part of the launch.
+constexpr int LN_THREADS = 256;
+constexpr int LN_WARPS = LN_THREADS / 32;
+constexpr int LN_MAXV = 8;  // float4 per thread: H <= 8192 (4 for H <= 4096)
 
-__device__ __forceinline__ float block_sum_128(float v, float* red) {
+__device__ __forceinline__ float block_sum(float v, float* red) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
   const int w = threadIdx.x >> 5;
   __syncthreads();  // red[] may still be read by a previous call
   if ((threadIdx.x & 31) == 0) red[w] = v;
   __syncthreads();
-  return (red[0] + red[1]) + (red[2] + red[3]);
+  float t = 0.f;
+#pragma unroll
+  for (int i = 0; i < LN_WARPS; ++i) t += red[i];
+  return t;
 }
 
 // With `out_lo` the result is also kept to about 16 significant bits as the
@@ -39,7 +45,7 @@ __global__ void __launch_bounds__(LN_THREADS) ln_modulate_kernel(
     const float* __restrict__ x, long long ldx, int rows, int H, const float* __restrict__ p0,
     const float* __restrict__ p1, float eps, __nv_bfloat16* __restrict__ out, long long ldo,
     __nv_bfloat16* __restrict__ out_lo) {
-  __shared__ float red[4];
+  __shared__ float red[LN_WARPS];
   const int row = blockIdx.x;
   if (row >= rows) return;
   const float4* xr = reinterpret_cast<const float4*>(x + (size_t)row * ldx);
@@ -55,7 +61,7 @@ __global__ void __launch_bounds__(LN_THREADS) ln_modulate_kernel(
     }
   }
   // RMSNorm keeps the mean (it divides by the root mean square instead)
-  const float mean = RMS ? 0.0f : block_sum_128(s, red) / (float)H;
+  const float mean = RMS ? 0.0f : block_sum(s, red) / (float)H;
   float ss = 0.f;
 #pragma unroll
   for (int i = 0; i < MAXV; ++i) {
@@ -65,7 +71,7 @@ __global__ void __launch_bounds__(LN_THREADS) ln_modulate_kernel(
       ss += (v[i].x * v[i].x + v[i].y * v[i].y) + (v[i].z * v[i].z + v[i].w * v[i].w);
     }
   }
-  const float rstd = 1.0f / sqrtf(block_sum_128(ss, red) / (float)H + eps);
+  const float rstd = 1.0f / sqrtf(block_sum(ss, red) / (float)H + eps);
   uint2* orow = reinterpret_cast<uint2*>(out + (size_t)row * ldo);
   const float4* a4 = reinterpret_cast<const float4*>(p0);
   const float4* b4 = reinterpret_cast<const float4*>(p1);
@@ -318,9 +324,9 @@ cudaError_t launch_ln_modulate(int mode, const float* x, long long ldx, int rows
   if (H > LN_THREADS * 4 * LN_MAXV || (H & 3)) return cudaErrorInvalidValue;
   const int grid = rows;
   if (grid == 0) return cudaSuccess;
-  const bool small = H <= LN_THREADS * 4 * 8;
+  const bool small = H <= LN_THREADS * 4 * 4;
 #define DIT_LN_LAUNCH(M, R)                                                                     \
-  (small ? (ln_modulate_kernel<M, R, 8><<<grid, LN_THREADS, 0, st>>>(x, ldx, rows, H, p0, p1, eps, \
+  (small ? (ln_modulate_kernel<M, R, 4><<<grid, LN_THREADS, 0, st>>>(x, ldx, rows, H, p0, p1, eps, \
                                                                      out, ldo, out_lo), 0)          \
          : (ln_modulate_kernel<M, R, LN_MAXV><<<grid, LN_THREADS, 0, st>>>(x, ldx, rows, H, p0, p1, \
                                                                            eps, out, ldo, out_lo), \
