@@ -78,7 +78,7 @@ constexpr int EPI_SMEM = 4 * 2 * EBUF_BYTES;
 template <int EPI>
 constexpr bool is_staged() {
   return EPI == EPI_BF16 || EPI == EPI_SWIGLU || EPI == EPI_GEGLU || EPI == EPI_RESIDUAL ||
-         EPI == EPI_RESIDUAL_TANH || EPI == EPI_RESIDUAL_SIGMOID;
+         EPI == EPI_RESIDUAL_TANH || EPI == EPI_RESIDUAL_SIGMOID || EPI == EPI_QKV;
 }
 template <int EPI>
 constexpr size_t smem_bytes() {
@@ -223,9 +223,12 @@ __device__ __forceinline__ void tile_coords(const GemmParams& p, int t, int& m_b
 // ---------------------------------------------------------------- epilogues
 // row: this thread's output row; row0: the first row of its warp's slab.
 template <int EPI, int HD, bool F8>
+// tmO: the output map of the staged epilogues (q/k heads for EPI_QKV); tmV:
+// the transposed v of EPI_QKV.
 __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const CUtensorMap* tmO,
-                                              EpiStage& es, uint32_t tbase, int row, int row0,
-                                              int lane, int n_blk) {
+                                              const CUtensorMap* tmV, EpiStage& es,
+                                              uint32_t tbase, int row, int row0, int lane,
+                                              int n_blk) {
   const bool row_ok = row < p.M;
   float rs = 1.0f;
   if constexpr (F8) rs = row_ok ? __ldg(p.sa + row) : 0.0f;
@@ -390,7 +393,6 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const CUtenso
 #pragma unroll
       for (int c = 0; c < HD / 32; ++c)
         tmem_ld32(tbase + hh * HD + c * 32, *reinterpret_cast<float(*)[32]>(&v[c * 32]));
-      if (!row_ok) continue;
       if constexpr (F8) {
 #pragma unroll
         for (int c = 0; c < HD / 32; ++c)
@@ -422,18 +424,53 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const CUtenso
         }
         if (!q.rope_first) rope_row<HD>(v, q, row);
         // head-major: one head's rows are contiguous, so an attention tile of
-        // 128 tokens x d is one contiguous block
-        __nv_bfloat16* dst = q.qk + ((size_t)head * p.M + row) * HD;
+        // 128 tokens x d is one contiguous block.  Staged 64 channels at a
+        // time and stored by TMA as boxes (64, 32 rows) of the map
+        // [head][token][d]; rows past M are not written.
 #pragma unroll
-        for (int c = 0; c < HD / 32; ++c)
-          store_bf16x32(dst + c * 32, *reinterpret_cast<float(*)[32]>(&v[c * 32]));
+        for (int c = 0; c < HD / 64; ++c) {
+          uint8_t* bf = ebuf_acquire(es, lane);
+#pragma unroll
+          for (int qq = 0; qq < 8; ++qq) ebuf_put16(bf, lane, qq, pack_bf16x8(v + c * 64 + 8 * qq));
+          ebuf_release(es);
+          if (lane == 0 && row0 < p.M) {  // a slab wholly below M stores nothing
+            tma_store_3d(tmO, bf, c * 64, row0, head);
+            bulk_commit();
+          }
+        }
       } else {
         const int g = head - q.nh - q.nkv;
-        const int seq = row / q.s_len;
-        const int j = row - seq * q.s_len;
-        __nv_bfloat16* dst = q.vt + ((size_t)(seq * q.nkv + g) * HD) * q.s_pad + j;
+        const int seq0 = row0 / q.s_len;
+        const int j0 = row0 - seq0 * q.s_len;
+        // the slab's existing rows (< M) all in one sequence, starting on a
+        // 16-byte boundary of the transposed row: one TMA box (32 tokens x
+        // d channels) from a transposed staging tile [d][32] filling both
+        // staging buffers of this warp
+        const int rows_end = min(row0 + 32, p.M);
+        if (row0 >= p.M) {
+          // a slab wholly below M stores nothing
+        } else if (j0 % 8 == 0 && rows_end <= (seq0 + 1) * q.s_len) {
+          if (lane == 0) bulk_wait_read<0>();   // both staging buffers free
+          __syncwarp();
+          __nv_bfloat16* tb = reinterpret_cast<__nv_bfloat16*>(es.buf);
 #pragma unroll
-        for (int c = 0; c < HD; ++c) dst[(size_t)c * q.s_pad] = __float2bfloat16_rn(v[c]);
+          for (int c = 0; c < HD; ++c) tb[c * 32 + lane] = __float2bfloat16_rn(v[c]);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(tmV, tb, j0, (seq0 * q.nkv + g) * HD);
+            bulk_commit();
+            bulk_wait_read<0>();   // the next acquire finds both buffers free
+          }
+          __syncwarp();
+          es.cur = 0;
+        } else if (row_ok) {
+          const int seq = row / q.s_len;
+          const int j = row - seq * q.s_len;
+          __nv_bfloat16* dst = q.vt + ((size_t)(seq * q.nkv + g) * HD) * q.s_pad + j;
+#pragma unroll
+          for (int c = 0; c < HD; ++c) dst[(size_t)c * q.s_pad] = __float2bfloat16_rn(v[c]);
+        }
       }
     }
   }
@@ -443,7 +480,8 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const CUtenso
 template <int EPI, int HD, bool F8>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                const __grid_constant__ CUtensorMap tmO, const GemmParams p) {
+                const __grid_constant__ CUtensorMap tmO, const __grid_constant__ CUtensorMap tmV,
+                const GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -586,8 +624,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       tc_fence_after();
       const uint32_t tbase = tmem_base + (uint32_t)(acc * BN) + ((uint32_t)(quarter * 32) << 16);
       const int row_base = m_blk * PM + (int)rank * BM;
-      epilogue_tile<EPI, HD, F8>(p, &tmO, es, tbase, row_base + r_in, row_base + quarter * 32,
-                                 lane, n_blk);
+      epilogue_tile<EPI, HD, F8>(p, &tmO, &tmV, es, tbase, row_base + r_in,
+                                 row_base + quarter * 32, lane, n_blk);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(acc ? te1 : te0);
@@ -608,7 +646,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 // no more pairs than can be resident at once (queried once per device).
 template <int EPI, int HD, bool F8>
 cudaError_t launch_impl(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& to,
-                        const GemmParams& p, int tiles, int sm_count, cudaStream_t st) {
+                        const CUtensorMap& tv, const GemmParams& p, int tiles, int sm_count,
+                        cudaStream_t st) {
   static int max_pairs[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -640,7 +679,7 @@ cudaError_t launch_impl(const CUtensorMap& ta, const CUtensorMap& tb, const CUte
   }
   const int pairs = tiles < max_pairs[dev] ? tiles : max_pairs[dev];
   cfg.gridDim = dim3(2 * pairs, 1, 1);
-  cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_kernel<EPI, HD, F8>, ta, tb, to, p);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_kernel<EPI, HD, F8>, ta, tb, to, tv, p);
   count_launch();
   return e != cudaSuccess ? e : cudaGetLastError();
 }
@@ -680,6 +719,28 @@ cudaError_t launch_gemm_t(int epi, int hd, const void* A, long long lda, const v
     const uint32_t box[2] = {resid ? 32u : 64u, 32u};
     if (!make_tmap(&to, oes, p.out, 2, dims, strides, box)) return cudaErrorInvalidValue;
   }
+  // EPI_QKV: q/k heads as [head][token][d] (boxes of 64 channels x 32 tokens
+  // x 1 head, 128-byte swizzle like the staging buffers), and v transposed
+  // [seq][g][c][s_pad] as a 2-D view x = token (s_len of s_pad columns),
+  // y = (seq nkv + g) d + c (boxes of 32 tokens x d channels, unswizzled)
+  CUtensorMap tv = ta;
+  if (epi == EPI_QKV) {
+    const QkvEpi& q = p.qkv;
+    if (hd != 64 && hd != 128) return cudaErrorInvalidValue;
+    {
+      const uint64_t dims[3] = {(uint64_t)hd, (uint64_t)p.M, (uint64_t)(q.nh + q.nkv)};
+      const uint64_t strides[2] = {(uint64_t)hd * 2, (uint64_t)p.M * hd * 2};
+      const uint32_t box[3] = {64u, 32u, 1u};
+      if (!make_tmap(&to, 2, q.qk, 3, dims, strides, box)) return cudaErrorInvalidValue;
+    }
+    {
+      const uint64_t n_seqs = (uint64_t)(p.M / q.s_len);
+      const uint64_t dims[2] = {(uint64_t)q.s_len, n_seqs * q.nkv * hd};
+      const uint64_t strides[1] = {(uint64_t)q.s_pad * 2};
+      const uint32_t box[2] = {32u, (uint32_t)hd};
+      if (!make_tmap(&tv, 2, q.vt, 2, dims, strides, box, false)) return cudaErrorInvalidValue;
+    }
+  }
   p.num_m = (p.M + PM - 1) / PM;
   p.num_n = glu ? p.N / 128 : (p.N + BN - 1) / BN;
   // raster groups of row blocks whose A rows take at most ~40 MB of L2
@@ -693,20 +754,20 @@ cudaError_t launch_gemm_t(int epi, int hd, const void* A, long long lda, const v
   const int tiles = p.num_m * p.num_n;
   const int sms = ds->sm_count;
   switch (epi) {
-    case EPI_BF16: return launch_impl<EPI_BF16, 0, F8>(ta, tb, to, p, tiles, sms, st);
-    case EPI_F32_BIAS: return launch_impl<EPI_F32_BIAS, 0, F8>(ta, tb, to, p, tiles, sms, st);
-    case EPI_RESIDUAL: return launch_impl<EPI_RESIDUAL, 0, F8>(ta, tb, to, p, tiles, sms, st);
-    case EPI_SWIGLU: return launch_impl<EPI_SWIGLU, 0, F8>(ta, tb, to, p, tiles, sms, st);
-    case EPI_GEGLU: return launch_impl<EPI_GEGLU, 0, F8>(ta, tb, to, p, tiles, sms, st);
-    case EPI_RESIDUAL_TANH: return launch_impl<EPI_RESIDUAL_TANH, 0, F8>(ta, tb, to, p, tiles, sms, st);
+    case EPI_BF16: return launch_impl<EPI_BF16, 0, F8>(ta, tb, to, tv, p, tiles, sms, st);
+    case EPI_F32_BIAS: return launch_impl<EPI_F32_BIAS, 0, F8>(ta, tb, to, tv, p, tiles, sms, st);
+    case EPI_RESIDUAL: return launch_impl<EPI_RESIDUAL, 0, F8>(ta, tb, to, tv, p, tiles, sms, st);
+    case EPI_SWIGLU: return launch_impl<EPI_SWIGLU, 0, F8>(ta, tb, to, tv, p, tiles, sms, st);
+    case EPI_GEGLU: return launch_impl<EPI_GEGLU, 0, F8>(ta, tb, to, tv, p, tiles, sms, st);
+    case EPI_RESIDUAL_TANH: return launch_impl<EPI_RESIDUAL_TANH, 0, F8>(ta, tb, to, tv, p, tiles, sms, st);
     case EPI_RESIDUAL_SIGMOID:
-      return launch_impl<EPI_RESIDUAL_SIGMOID, 0, F8>(ta, tb, to, p, tiles, sms, st);
+      return launch_impl<EPI_RESIDUAL_SIGMOID, 0, F8>(ta, tb, to, tv, p, tiles, sms, st);
     case EPI_EULER:
-      if constexpr (!F8) return launch_impl<EPI_EULER, 0, F8>(ta, tb, to, p, tiles, sms, st);
+      if constexpr (!F8) return launch_impl<EPI_EULER, 0, F8>(ta, tb, to, tv, p, tiles, sms, st);
       return cudaErrorInvalidValue;
     case EPI_QKV:
-      if (hd == 64) return launch_impl<EPI_QKV, 64, F8>(ta, tb, to, p, tiles, sms, st);
-      if (hd == 128) return launch_impl<EPI_QKV, 128, F8>(ta, tb, to, p, tiles, sms, st);
+      if (hd == 64) return launch_impl<EPI_QKV, 64, F8>(ta, tb, to, tv, p, tiles, sms, st);
+      if (hd == 128) return launch_impl<EPI_QKV, 128, F8>(ta, tb, to, tv, p, tiles, sms, st);
       return cudaErrorInvalidValue;
     default: return cudaErrorInvalidValue;
   }
