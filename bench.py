@@ -431,7 +431,7 @@ def secondary_workloads(dit, synth, dev, args, tc_peak, tc_sustained, hbm_peak):
     fin = torch.empty(2, wl.hidden, device=dev)
     scratch = torch.empty(wl.t_dim + 2 * wl.hidden, device=dev)
     dit.dit_timestep_conditioning(cfg, model, sig[0], mod, fin, scratch)
-    rc = torch.empty(wl.n_tokens, wl.head_dim // 2, device=dev)
+    rc = torch.empty(wl.head_dim // 2, wl.n_tokens, device=dev)
     rs = torch.empty_like(rc)
     dit.dit_rope_table_grid(wl.grid_h, wl.grid_w, wl.n_txt, wl.rope_axes, wl.rope_theta, rc, rs)
     x = torch.randn(wl.n_tokens, wl.hidden, device=dev)
@@ -455,7 +455,7 @@ def secondary_workloads(dit, synth, dev, args, tc_peak, tc_sustained, hbm_peak):
     blocks = [dit.DeviceBlock(synth.block_weights(wl, li, seed=0, device=dev), dev)
               for li in range(wl.n_layers)]
     cfg = dit.block_config_from(wl)
-    rc = torch.empty(wl.seq_len, wl.head_dim // 2, device=dev)
+    rc = torch.empty(wl.head_dim // 2, wl.seq_len, device=dev)
     rs = torch.empty_like(rc)
     dit.dit_rope_table_vit(wl.grid_h, wl.grid_w, wl.n_prefix, wl.head_dim, 10000.0, rc, rs)
     bws = dit.workspace(dit.dit_block_workspace_bytes(cfg, wl.n_tokens, wl.n_seqs), dev)
@@ -501,7 +501,7 @@ def run_profile_stage(args):
     fin = torch.empty(2, wl.hidden, device=dev)
     scratch = torch.empty(wl.t_dim + 2 * wl.hidden, device=dev)
     dit.dit_timestep_conditioning(cfg, model, 0.5, mod, fin, scratch)
-    rc = torch.empty(wl.n_tokens, wl.head_dim // 2, device=dev)
+    rc = torch.empty(wl.head_dim // 2, wl.n_tokens, device=dev)
     rs = torch.empty_like(rc)
     dit.dit_rope_table_grid(wl.grid_h, wl.grid_w, wl.n_txt, wl.rope_axes, wl.rope_theta, rc, rs)
     x = torch.randn(wl.n_tokens, wl.hidden, device=dev)
@@ -634,7 +634,7 @@ def run_ours(args, rank, world, local):
     fin = torch.empty(2, wl.hidden, device=dev)
     scratch = torch.empty(wl.t_dim + 2 * wl.hidden, device=dev)
     dit.dit_timestep_conditioning(cfg, model, sig[0], mod, fin, scratch)
-    rc = torch.empty(wl.n_tokens, wl.head_dim // 2, device=dev)
+    rc = torch.empty(wl.head_dim // 2, wl.n_tokens, device=dev)
     rs = torch.empty_like(rc)
     dit.dit_rope_table_grid(wl.grid_h, wl.grid_w, wl.n_txt, wl.rope_axes, wl.rope_theta, rc, rs)
     x = torch.randn(wl.n_tokens, wl.hidden, device=dev)

@@ -26,6 +26,12 @@ PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// The per-head norm parameters, read as float4 by the QKV epilogue.
+bool qk_norm_params_ok(const dit_block_weights* w) {
+  return w->q_g && w->q_b && w->k_g && w->k_b && aligned16(w->q_g) && aligned16(w->q_b) &&
+         aligned16(w->k_g) && aligned16(w->k_b);
+}
+
 size_t align256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
 
 dit_status cuda_status(cudaError_t e) { return e == cudaSuccess ? DIT_OK : DIT_ECUDA; }
@@ -339,7 +345,7 @@ dit_status check_block_weights(const dit_block_config* c, const dit_block_weight
     for (const float* p : sc)
       if (!p || !aligned16(p)) return DIT_EINVAL;
   }
-  if (c->qk_norm && (!w->q_g || !w->q_b || !w->k_g || !w->k_b)) return DIT_EINVAL;
+  if (c->qk_norm && !qk_norm_params_ok(w)) return DIT_EINVAL;
   if (!c->adaln) {
     if (!w->ln1_g || !w->ln1_b || !w->ln2_g || !w->ln2_b) return DIT_EINVAL;
     if (!aligned16(w->ln1_g) || !aligned16(w->ln1_b) || !aligned16(w->ln2_g) ||
@@ -705,7 +711,7 @@ dit_status dit_qkv_rope(const dit_block_config* cfg, const dit_block_weights* w,
   dit_status s = check_block_config(cfg);
   if (s != DIT_OK) return s;
   if (!w || !w->w_qkv || !aligned16(w->w_qkv)) return DIT_EINVAL;
-  if (cfg->qk_norm && (!w->q_g || !w->q_b || !w->k_g || !w->k_b)) return DIT_EINVAL;
+  if (cfg->qk_norm && !qk_norm_params_ok(w)) return DIT_EINVAL;
   if (!a || !qk || !vt || !rope_cos || !rope_sin || n_tokens <= 0 || n_seqs <= 0 ||
       n_tokens % n_seqs)
     return DIT_EINVAL;
@@ -728,7 +734,7 @@ dit_status dit_qkv_rope_e4m3(const dit_block_config* cfg, const dit_block_weight
   if (cfg->linear_format != DIT_LINEAR_W8A8_H256) return DIT_EINVAL;
   if (!w || !w->w_qkv || !aligned16(w->w_qkv) || !w->w_qkv_scale || !aligned16(w->w_qkv_scale))
     return DIT_EINVAL;
-  if (cfg->qk_norm && (!w->q_g || !w->q_b || !w->k_g || !w->k_b)) return DIT_EINVAL;
+  if (cfg->qk_norm && !qk_norm_params_ok(w)) return DIT_EINVAL;
   if (!a || !a_scales || !qk || !vt || !rope_cos || !rope_sin || n_tokens <= 0 || n_seqs <= 0 ||
       n_tokens % n_seqs)
     return DIT_EINVAL;

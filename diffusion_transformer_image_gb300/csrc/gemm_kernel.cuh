@@ -158,30 +158,129 @@ constexpr bool is_residual() {
   return EPI == EPI_RESIDUAL || EPI == EPI_RESIDUAL_TANH || EPI == EPI_RESIDUAL_SIGMOID;
 }
 
-// Rotates the pairs of one head row by the RoPE table row of its token:
-// pairs (2k, 2k+1) or (k, k + HD/2), angle k.
+// Rotates the pairs of one head row by the RoPE table column of its token:
+// pairs (2k, 2k+1) or (k, k + HD/2), angle k.  The tables are pair-major
+// [HD/2][s_len], so the 32 lanes of a warp (32 consecutive tokens) read one
+// pair's entries in one coalesced request.
 template <int HD>
 __device__ __forceinline__ void rope_row(float (&v)[HD], const QkvEpi& q, int row) {
   const int trow = row % q.s_len;
-  const float4* cs = reinterpret_cast<const float4*>(q.rcos + (size_t)trow * (HD / 2));
-  const float4* sn = reinterpret_cast<const float4*>(q.rsin + (size_t)trow * (HD / 2));
+  const float* cs = q.rcos + trow;
+  const float* sn = q.rsin + trow;
+  constexpr int KC = 16;  // pairs whose table entries are loaded together
 #pragma unroll
-  for (int k4 = 0; k4 < HD / 8; ++k4) {
-    const float4 c4 = __ldg(cs + k4), s4 = __ldg(sn + k4);
-    const float cc[4] = {c4.x, c4.y, c4.z, c4.w};
-    const float ssn[4] = {s4.x, s4.y, s4.z, s4.w};
+  for (int k0 = 0; k0 < HD / 2; k0 += KC) {
+    float c[KC], s[KC];
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const int k = 4 * k4 + e;
+    for (int e = 0; e < KC; ++e) {
+      c[e] = __ldg(cs + (size_t)(k0 + e) * q.s_len);
+      s[e] = __ldg(sn + (size_t)(k0 + e) * q.s_len);
+    }
+#pragma unroll
+    for (int e = 0; e < KC; ++e) {
+      const int k = k0 + e;
       if (q.rope_half) {
         const float a = v[k], bb = v[k + HD / 2];
-        v[k] = a * cc[e] - bb * ssn[e];
-        v[k + HD / 2] = a * ssn[e] + bb * cc[e];
+        v[k] = a * c[e] - bb * s[e];
+        v[k + HD / 2] = a * s[e] + bb * c[e];
       } else {
         const float a = v[2 * k], bb = v[2 * k + 1];
-        v[2 * k] = a * cc[e] - bb * ssn[e];
-        v[2 * k + 1] = a * ssn[e] + bb * cc[e];
+        v[2 * k] = a * c[e] - bb * s[e];
+        v[2 * k + 1] = a * s[e] + bb * c[e];
       }
+    }
+  }
+}
+
+// The 16 pairs j*16 .. j*16+15 of one head row as two arrays (first and
+// second element of each pair): interleaved pairs (2k, 2k+1) come from the
+// 32 columns from 32 j, rotate-half pairs (k, k + HD/2) from the 16 columns
+// from 16 j and the 16 from HD/2 + 16 j.  pair_cols reads a per-column
+// vector (gains, biases, column scales) the same way.
+template <int HD>
+__device__ __forceinline__ void pair_cols(const float* vec, bool half, int j, float (&a)[16],
+                                          float (&b)[16]) {
+  if (half) {
+    const float4* pa = reinterpret_cast<const float4*>(vec + 16 * j);
+    const float4* pb = reinterpret_cast<const float4*>(vec + HD / 2 + 16 * j);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float4 x = __ldg(pa + i), y = __ldg(pb + i);
+      a[4 * i] = x.x; a[4 * i + 1] = x.y; a[4 * i + 2] = x.z; a[4 * i + 3] = x.w;
+      b[4 * i] = y.x; b[4 * i + 1] = y.y; b[4 * i + 2] = y.z; b[4 * i + 3] = y.w;
+    }
+  } else {
+    const float4* p4 = reinterpret_cast<const float4*>(vec + 32 * j);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float4 x = __ldg(p4 + i);
+      a[2 * i] = x.x; b[2 * i] = x.y; a[2 * i + 1] = x.z; b[2 * i + 1] = x.w;
+    }
+  }
+}
+
+template <int HD>
+__device__ __forceinline__ void tmem_pairs(uint32_t hb, bool half, int j, float (&a)[16],
+                                           float (&b)[16]) {
+  if (half) {
+    tmem_ld16(hb + 16 * j, a);
+    tmem_ld16(hb + HD / 2 + 16 * j, b);
+  } else {
+    float x[32];
+    tmem_ld32(hb + 32 * j, x);
+#pragma unroll
+    for (int e = 0; e < 16; ++e) {
+      a[e] = x[2 * e];
+      b[e] = x[2 * e + 1];
+    }
+  }
+}
+
+// Rotates pairs 16 j .. 16 j + 15 of the token at table column trow.
+__device__ __forceinline__ void rope_pairs(float (&a)[16], float (&b)[16], const QkvEpi& q,
+                                           int trow, int j) {
+  const float* cs = q.rcos + (size_t)(16 * j) * q.s_len + trow;
+  const float* sn = q.rsin + (size_t)(16 * j) * q.s_len + trow;
+  float c[16], s[16];
+#pragma unroll
+  for (int e = 0; e < 16; ++e) {
+    c[e] = __ldg(cs + (size_t)e * q.s_len);
+    s[e] = __ldg(sn + (size_t)e * q.s_len);
+  }
+#pragma unroll
+  for (int e = 0; e < 16; ++e) {
+    const float x = a[e], y = b[e];
+    a[e] = x * c[e] - y * s[e];
+    b[e] = x * s[e] + y * c[e];
+  }
+}
+
+// Writes the 16 pairs j of a head row as bf16 into the staging buffers of
+// the warp (buffer = 64-column box of the head, 128-byte swizzled rows).
+template <int HD>
+__device__ __forceinline__ void stage_pairs(uint8_t* buf, int lane, bool half, int j,
+                                            const float (&a)[16], const float (&b)[16]) {
+  if (half) {
+    const int ca = 16 * j, cb = HD / 2 + 16 * j;
+    uint8_t* ba = buf + (ca >> 6) * EBUF_BYTES;
+    uint8_t* bb = buf + (cb >> 6) * EBUF_BYTES;
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      ebuf_put16(ba, lane, ((ca & 63) >> 3) + i, pack_bf16x8(a + 8 * i));
+      ebuf_put16(bb, lane, ((cb & 63) >> 3) + i, pack_bf16x8(b + 8 * i));
+    }
+  } else {
+    const int c0 = 32 * j;
+    uint8_t* bx = buf + (c0 >> 6) * EBUF_BYTES;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      float x[8];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        x[2 * e] = a[4 * i + e];
+        x[2 * e + 1] = b[4 * i + e];
+      }
+      ebuf_put16(bx, lane, ((c0 & 63) >> 3) + i, pack_bf16x8(x));
     }
   }
 }
@@ -388,57 +487,100 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const CUtenso
       const int col0 = n_blk * BN + hh * HD;
       if (col0 >= p.N) break;
       const int head = col0 / HD;
-      float v[HD];
-      __syncwarp();
-#pragma unroll
-      for (int c = 0; c < HD / 32; ++c)
-        tmem_ld32(tbase + hh * HD + c * 32, *reinterpret_cast<float(*)[32]>(&v[c * 32]));
-      if constexpr (F8) {
-#pragma unroll
-        for (int c = 0; c < HD / 32; ++c)
-          scale_cols(*reinterpret_cast<float(*)[32]>(&v[c * 32]), rs, p.sb, col0 + c * 32, p.N);
-      }
+      const uint32_t hb = tbase + hh * HD;   // this head's accumulator columns
       if (head < q.nh + q.nkv) {
         const bool is_q = head < q.nh;
         const float* g = is_q ? q.qg : q.kg;
         const float* b = is_q ? q.qb : q.kb;
-        if (q.rope_first) rope_row<HD>(v, q, row);
+        const int trow = row % q.s_len;
+        // pass 1: the row's norm statistics over all HD values (of the
+        // rotated row when the rotation comes first), in eight interleaved
+        // partial sums
+        float mean = 0.f, rstd = 1.f;
         if (g != nullptr) {
-          // per-head LayerNorm or RMSNorm over the head_dim values of this row
-          float mean = 0.f;
-          if (!q.rms) {
-            float s = 0.f;
+          float v[HD];
+          __syncwarp();
 #pragma unroll
-            for (int i = 0; i < HD; ++i) s += v[i];
-            mean = s * (1.0f / HD);
+          for (int c = 0; c < HD / 32; ++c)
+            tmem_ld32(hb + c * 32, *reinterpret_cast<float(*)[32]>(&v[c * 32]));
+          if constexpr (F8) {
+#pragma unroll
+            for (int c = 0; c < HD / 32; ++c)
+              scale_cols(*reinterpret_cast<float(*)[32]>(&v[c * 32]), rs, p.sb, col0 + c * 32,
+                         p.N);
           }
-          float ss = 0.f;
+          if (q.rope_first) rope_row<HD>(v, q, row);
+          if (!q.rms) {
+            float sm[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int i = 0; i < HD; ++i) sm[i & 7] += v[i];
+            mean = (((sm[0] + sm[1]) + (sm[2] + sm[3])) + ((sm[4] + sm[5]) + (sm[6] + sm[7]))) *
+                   (1.0f / HD);
+          }
+          float ss[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
           for (int i = 0; i < HD; ++i) {
-            v[i] -= mean;
-            ss = fmaf(v[i], v[i], ss);
+            const float d = v[i] - mean;
+            ss[i & 7] = fmaf(d, d, ss[i & 7]);
           }
-          const float rstd = 1.0f / sqrtf(ss * (1.0f / HD) + q.eps);
-#pragma unroll
-          for (int i = 0; i < HD; ++i) v[i] = fmaf(v[i] * rstd, __ldg(g + i), __ldg(b + i));
+          const float var =
+              (((ss[0] + ss[1]) + (ss[2] + ss[3])) + ((ss[4] + ss[5]) + (ss[6] + ss[7]))) *
+              (1.0f / HD);
+          rstd = 1.0f / sqrtf(var + q.eps);
         }
-        if (!q.rope_first) rope_row<HD>(v, q, row);
-        // head-major: one head's rows are contiguous, so an attention tile of
-        // 128 tokens x d is one contiguous block.  Staged 64 channels at a
-        // time and stored by TMA as boxes (64, 32 rows) of the map
-        // [head][token][d]; rows past M are not written.
+        // pass 2: 16 pairs at a time from TMEM again: scale, norm and
+        // rotation in the block's order, bf16 into the staging buffers (one
+        // per 64-column box); then one TMA box (64, 32 rows) per 64 columns
+        // of the head-major map [head][token][d].  Rows past M are not
+        // written.
+        if (lane == 0) bulk_wait_read<0>();   // both staging buffers free
+        __syncwarp();
 #pragma unroll
-        for (int c = 0; c < HD / 64; ++c) {
-          uint8_t* bf = ebuf_acquire(es, lane);
+        for (int j = 0; j < HD / 32; ++j) {
+          float pa[16], pb[16];
+          tmem_pairs<HD>(hb, q.rope_half, j, pa, pb);
+          if constexpr (F8) {
+            float sa[16], sb[16];
+            pair_cols<HD>(p.sb + col0, q.rope_half, j, sa, sb);
 #pragma unroll
-          for (int qq = 0; qq < 8; ++qq) ebuf_put16(bf, lane, qq, pack_bf16x8(v + c * 64 + 8 * qq));
-          ebuf_release(es);
-          if (lane == 0 && row0 < p.M) {  // a slab wholly below M stores nothing
-            tma_store_3d(tmO, bf, c * 64, row0, head);
-            bulk_commit();
+            for (int e = 0; e < 16; ++e) {
+              pa[e] *= rs * sa[e];
+              pb[e] *= rs * sb[e];
+            }
           }
+          if (q.rope_first) rope_pairs(pa, pb, q, trow, j);
+          if (g != nullptr) {
+            float ga[16], gb[16], ba[16], bb[16];
+            pair_cols<HD>(g, q.rope_half, j, ga, gb);
+            pair_cols<HD>(b, q.rope_half, j, ba, bb);
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              pa[e] = fmaf((pa[e] - mean) * rstd, ga[e], ba[e]);
+              pb[e] = fmaf((pb[e] - mean) * rstd, gb[e], bb[e]);
+            }
+          }
+          if (!q.rope_first) rope_pairs(pa, pb, q, trow, j);
+          stage_pairs<HD>(es.buf, lane, q.rope_half, j, pa, pb);
         }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0 && row0 < p.M) {  // a slab wholly below M stores nothing
+#pragma unroll
+          for (int c = 0; c < HD / 64; ++c) tma_store_3d(tmO, es.buf + c * EBUF_BYTES, c * 64, row0, head);
+          bulk_commit();
+        }
+        es.cur = 0;
       } else {
+        float v[HD];
+        __syncwarp();
+#pragma unroll
+        for (int c = 0; c < HD / 32; ++c)
+          tmem_ld32(hb + c * 32, *reinterpret_cast<float(*)[32]>(&v[c * 32]));
+        if constexpr (F8) {
+#pragma unroll
+          for (int c = 0; c < HD / 32; ++c)
+            scale_cols(*reinterpret_cast<float(*)[32]>(&v[c * 32]), rs, p.sb, col0 + c * 32, p.N);
+        }
         const int g = head - q.nh - q.nkv;
         const int seq0 = row0 / q.s_len;
         const int j0 = row0 - seq0 * q.s_len;
@@ -460,10 +602,8 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const CUtenso
           if (lane == 0) {
             tma_store_2d(tmV, tb, j0, (seq0 * q.nkv + g) * HD);
             bulk_commit();
-            bulk_wait_read<0>();   // the next acquire finds both buffers free
           }
-          __syncwarp();
-          es.cur = 0;
+          es.cur = 0;   // every staged write of this epilogue first waits for both buffers
         } else if (row_ok) {
           const int seq = row / q.s_len;
           const int j = row - seq * q.s_len;

@@ -51,7 +51,7 @@ struct QkvEpi {
   int s_len, s_pad;
   int nh, nkv;
   const float *qg, *qb, *kg, *kb;   // null when there is no qk norm
-  const float *rcos, *rsin;         // [s_len, hd/2]
+  const float *rcos, *rsin;         // pair-major [hd/2][s_len]
   int rope_half;                    // 0: pairs (2k, 2k+1); 1: pairs (k, k + hd/2)
   int rms;                          // qk-norm is RMSNorm instead of LayerNorm
   int rope_first;                   // RoPE before the qk-norm

@@ -193,7 +193,9 @@ __global__ void sinusoid_kernel(float T, int dim, float* out) {
 // token layout; section VII, Decision 3).  Pair k of the head vector belongs
 // to axis a when it falls in that axis's chunk; it turns by
 // pos_a * theta^(-2 j / axes[a]) (j = pair index inside the chunk), the
-// frequency rounded to float from double, the product in float.
+// frequency rounded to float from double, the product in float.  Tables are
+// pair-major, [d/2][n]: the QKV epilogue holds one token per lane, so a warp
+// reads 32 consecutive tokens of one pair in one coalesced request.
 struct Axes3 {
   int a0, a1, a2;
 };
@@ -205,8 +207,8 @@ __global__ void rope_grid_kernel(int grid_h, int grid_w, int n_txt, const int* _
   const int n_img = grid_h * grid_w;
   for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total;
        i += (long long)gridDim.x * blockDim.x) {
-    const int t = (int)(i / half_d);
-    const int k = (int)(i - (long long)t * half_d);
+    const int k = (int)(i / n);
+    const int t = (int)(i - (long long)k * n);
     int p0, p1, p2;
     if (pos) {
       p0 = pos[3 * t];
@@ -238,15 +240,15 @@ __global__ void rope_grid_kernel(int grid_h, int grid_w, int n_txt, const int* _
 
 // Rotate-half tables of the pre-norm ViT: prefix tokens unrotated, patch
 // (r, c): pair k < d/4 turns by r w_k, pair d/4 + k by c w_k,
-// w_k = base^(-k / (d/4)).
+// w_k = base^(-k / (d/4)).  Pair-major like the grid tables.
 __global__ void rope_vit_kernel(int grid_h, int grid_w, int n_prefix, int head_dim, float base,
                                 float* __restrict__ cos_out, float* __restrict__ sin_out) {
   const int half = head_dim / 2, q = head_dim / 4;
   const long long n = (long long)n_prefix + (long long)grid_h * grid_w;
   for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n * half;
        i += (long long)gridDim.x * blockDim.x) {
-    const int t = (int)(i / half);
-    const int k = (int)(i - (long long)t * half);
+    const int k = (int)(i / n);
+    const int t = (int)(i - (long long)k * n);
     float ang = 0.0f;
     if (t >= n_prefix) {
       const int pidx = t - n_prefix;

@@ -374,6 +374,7 @@ def dit_timestep_conditioning_noalloc(cfg: ModelConfig, w: DeviceModel, sigma: f
 
 def dit_rope_table_grid(grid_h: int, grid_w: int, n_txt: int, axes: Sequence[int], theta: float,
                         cos_out, sin_out, stream=None):
+    """cos_out, sin_out: device fp32 [d/2, grid_h*grid_w + n_txt] (pair-major)."""
     ax = (c_int32 * 3)(*axes)
     _check(lib.dit_rope_table_grid(grid_h, grid_w, n_txt, ax, theta, _ptr(cos_out), _ptr(sin_out),
                                    _stream(stream)), "dit_rope_table_grid")
@@ -381,6 +382,7 @@ def dit_rope_table_grid(grid_h: int, grid_w: int, n_txt: int, axes: Sequence[int
 
 def dit_rope_table_pos(pos: torch.Tensor, axes: Sequence[int], theta: float, cos_out, sin_out,
                        stream=None):
+    """cos_out, sin_out: device fp32 [d/2, n] (pair-major) for pos [n, 3]."""
     ax = (c_int32 * 3)(*axes)
     _check(lib.dit_rope_table_pos(_ptr(pos), pos.shape[0], ax, theta, _ptr(cos_out), _ptr(sin_out),
                                   _stream(stream)), "dit_rope_table_pos")
@@ -388,6 +390,7 @@ def dit_rope_table_pos(pos: torch.Tensor, axes: Sequence[int], theta: float, cos
 
 def dit_rope_table_vit(grid_h: int, grid_w: int, n_prefix: int, head_dim: int, base: float,
                        cos_out, sin_out, stream=None):
+    """cos_out, sin_out: device fp32 [head_dim/2, n_prefix + grid_h*grid_w]."""
     _check(lib.dit_rope_table_vit(grid_h, grid_w, n_prefix, head_dim, base, _ptr(cos_out),
                                   _ptr(sin_out), _stream(stream)), "dit_rope_table_vit")
 

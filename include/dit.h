@@ -94,8 +94,8 @@ enum { DIT_LINEAR_BF16 = 0, DIT_LINEAR_W8A8_H256 = 1 };
  *   w_o    [H, n_heads d]
  *   w_gu   [2F, H]   gate rows first, then up rows
  *   w_down [H, F]
- * Norm parameters fp32: q_g, q_b, k_g, k_b [d] (used when qk_norm);
- * ln1_g, ln1_b, ln2_g, ln2_b [H] (used when adaln == 0).
+ * Norm parameters fp32, 16-byte aligned: q_g, q_b, k_g, k_b [d] (used when
+ * qk_norm); ln1_g, ln1_b, ln2_g, ln2_b [H] (used when adaln == 0).
  * With linear_format DIT_LINEAR_W8A8_H256 the four linears hold e4m3 codes
  * (one byte per element, same shapes) of the rotated weights and the four
  * scale pointers their fp32 per-row scales [rows]; otherwise the scales are
@@ -156,9 +156,10 @@ size_t dit_block_workspace_bytes(const dit_block_config* cfg, int32_t n_tokens,
  * n_seqs: tokens are n_seqs sequences of n_tokens / n_seqs rows; attention
  *      stays inside a sequence.
  * mod: device fp32 [6, H] (adaln) or NULL.
- * rope_cos, rope_sin: device fp32 [n_tokens / n_seqs, head_dim / 2], the
- *      rotation of pair k of the token at position t of its sequence (see
- *      dit_rope_table_grid / dit_rope_table_vit).
+ * rope_cos, rope_sin: device fp32 [head_dim / 2, n_tokens / n_seqs]
+ *      (pair-major), entry (k, t) the rotation of pair k of the token at
+ *      position t of its sequence (see dit_rope_table_grid /
+ *      dit_rope_table_vit).
  * workspace: device, >= dit_block_workspace_bytes(), else DIT_EWORKSPACE. */
 dit_status dit_block_forward(const dit_block_config* cfg, const dit_block_weights* w,
                              float* x, int32_t n_tokens, int32_t n_seqs,
@@ -231,7 +232,8 @@ dit_status dit_linear(int32_t epilogue, const void* a, int64_t lda, const void* 
  *   qk: device bf16 [n_heads + n_kv_heads][n_tokens][d], head-major: q heads
  *       then k heads, each head's rows contiguous
  *   vt: device bf16 [n_seqs, n_kv_heads, d, s_pad], v transposed per sequence,
- *       s_pad = round_up(n_tokens / n_seqs, 8); columns >= seq length unused. */
+ *       s_pad = round_up(n_tokens / n_seqs, 8); columns >= seq length unused.
+ * rope_cos, rope_sin: pair-major tables as for dit_block_forward. */
 dit_status dit_qkv_rope(const dit_block_config* cfg, const dit_block_weights* w,
                         const void* a, int32_t n_tokens, int32_t n_seqs,
                         const float* rope_cos, const float* rope_sin, void* qk,
@@ -342,12 +344,13 @@ dit_status dit_timestep_conditioning_noalloc(const dit_model_config* cfg,
  * (t / grid_w, t % grid_w) at position (n_txt, h, w); token t >= grid_h grid_w
  * is text token j = t - grid_h grid_w at (j, 0, 0).  Pair k of axis a (the
  * head vector split into consecutive chunks of rope_axes[a]) turns by
- * pos_a theta^(-2k / rope_axes[a]).  cos, sin: device fp32 [N, d/2]. */
+ * pos_a theta^(-2k / rope_axes[a]).  cos, sin: device fp32 [d/2, N]
+ * (pair-major: entry (k, t) at k N + t), N = grid_h grid_w + n_txt. */
 dit_status dit_rope_table_grid(int32_t grid_h, int32_t grid_w, int32_t n_txt,
                                const int32_t* rope_axes, float theta, float* cos_out,
                                float* sin_out, void* stream);
 
-/* Same from explicit positions: pos device int32 [n, 3]. */
+/* Same from explicit positions: pos device int32 [n, 3]; cos, sin [d/2, n]. */
 dit_status dit_rope_table_pos(const int32_t* pos, int32_t n, const int32_t* rope_axes,
                               float theta, float* cos_out, float* sin_out, void* stream);
 
@@ -355,7 +358,7 @@ dit_status dit_rope_table_pos(const int32_t* pos, int32_t n, const int32_t* rope
  * from tables): n_prefix unrotated tokens, then patch (r, c) of a grid_h x
  * grid_w grid; pair k < d/4 turns by r w_k, pair d/4 <= k < d/2 by
  * c w_(k - d/4), w_k = base^(-k / (d/4)).  cos, sin: device fp32
- * [n_prefix + grid_h grid_w, d/2]. */
+ * [d/2, n_prefix + grid_h grid_w] (pair-major). */
 dit_status dit_rope_table_vit(int32_t grid_h, int32_t grid_w, int32_t n_prefix,
                               int32_t head_dim, float base, float* cos_out,
                               float* sin_out, void* stream);

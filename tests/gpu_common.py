@@ -17,6 +17,13 @@ def npf(t: torch.Tensor) -> np.ndarray:
     return t.detach().to("cpu", torch.float32).numpy()
 
 
+def pair_major_tables(ang):
+    """Device cos/sin tables in the library's pair-major layout [d/2, n] from
+    oracle angles [n, d/2]."""
+    return (torch.from_numpy(np.ascontiguousarray(np.cos(ang).T)).to(dev()),
+            torch.from_numpy(np.ascontiguousarray(np.sin(ang).T)).to(dev()))
+
+
 def bf16_normal(shape, name, seed=7, std=1.0, mean=0.0) -> torch.Tensor:
     """Seeded bf16 CPU tensor (the oracle sees the same values widened)."""
     return synth.normal(shape, name, seed, std, mean).to(torch.bfloat16)

@@ -36,8 +36,8 @@ SMALL_BLOCKS = {
 
 def rope_tables(wl):
     half = wl.head_dim // 2
-    c = torch.empty(wl.seq_len, half, device=dev())
-    s = torch.empty(wl.seq_len, half, device=dev())
+    c = torch.empty(half, wl.seq_len, device=dev())
+    s = torch.empty(half, wl.seq_len, device=dev())
     if wl.rope_layout == "half":
         dit.dit_rope_table_vit(wl.grid_h, wl.grid_w, wl.n_prefix, wl.head_dim, 10000.0, c, s)
     else:
@@ -182,7 +182,7 @@ def test_block_token_permutation_equivariance():
     perm = torch.randperm(wl.n_tokens, generator=torch.Generator().manual_seed(3))
     outs = []
     for p in (torch.arange(wl.n_tokens), perm):
-        c = torch.empty(wl.n_tokens, wl.head_dim // 2, device=dev())
+        c = torch.empty(wl.head_dim // 2, wl.n_tokens, device=dev())
         s = torch.empty_like(c)
         dit.dit_rope_table_pos(pos[p].contiguous().to(dev()), wl.rope_axes, wl.rope_theta, c, s)
         xg = x[p].contiguous().to(dev())
@@ -205,7 +205,7 @@ def test_block_position_offset_invariance():
     deltas = []
     for off in ((0, 0, 0), (5, 3, 11)):
         p = (pos + torch.tensor(off, dtype=torch.int32)).contiguous().to(dev())
-        c = torch.empty(wl.n_tokens, wl.head_dim // 2, device=dev())
+        c = torch.empty(wl.head_dim // 2, wl.n_tokens, device=dev())
         s = torch.empty_like(c)
         dit.dit_rope_table_pos(p, wl.rope_axes, wl.rope_theta, c, s)
         xg = x.to(dev()).contiguous()

@@ -148,7 +148,7 @@ def test_vit_backbone_24_layers():
     cfg = dit.block_config_from(wl)
     ocfg, ang = oracle_block_config(wl), oracle_angles(wl)
     half = wl.head_dim // 2
-    rc = torch.empty(wl.seq_len, half, device=dev())
+    rc = torch.empty(half, wl.seq_len, device=dev())
     rs = torch.empty_like(rc)
     dit.dit_rope_table_vit(wl.grid_h, wl.grid_w, wl.n_prefix, wl.head_dim, 10000.0, rc, rs)
     ws = dit.workspace(dit.dit_block_workspace_bytes(cfg, wl.n_tokens, wl.n_seqs), dev())

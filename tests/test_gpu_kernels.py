@@ -5,7 +5,7 @@ import numpy as np
 import pytest
 import torch
 
-from gpu_common import bf16_normal, dev, npf
+from gpu_common import bf16_normal, dev, npf, pair_major_tables
 from oracle import dit_oracle as O
 
 pytestmark = pytest.mark.gpu
@@ -111,12 +111,12 @@ def test_sigmas_host_match_oracle():
                                              (5, 7, 3, (32, 48, 48))])
 def test_rope_table_grid(gh, gw, ntxt, axes):
     n, half = gh * gw + ntxt, sum(axes) // 2
-    c = torch.empty(n, half, device=dev())
-    s = torch.empty(n, half, device=dev())
+    c = torch.empty(half, n, device=dev())
+    s = torch.empty(half, n, device=dev())
     dit.dit_rope_table_grid(gh, gw, ntxt, axes, 256.0, c, s)
-    ang = O.rope_angles_3d(O.position_ids(gh, gw, ntxt), axes, 256.0)
-    np.testing.assert_allclose(npf(c), np.cos(ang), atol=2e-6, rtol=0)
-    np.testing.assert_allclose(npf(s), np.sin(ang), atol=2e-6, rtol=0)
+    ang = O.rope_angles_3d(O.position_ids(gh, gw, ntxt), axes, 256.0)   # [n, half]
+    np.testing.assert_allclose(npf(c), np.cos(ang).T, atol=2e-6, rtol=0)
+    np.testing.assert_allclose(npf(s), np.sin(ang).T, atol=2e-6, rtol=0)
     # the same table from explicit positions
     pos = torch.from_numpy(O.position_ids(gh, gw, ntxt)).to(dev())
     c2 = torch.empty_like(c)
@@ -126,12 +126,12 @@ def test_rope_table_grid(gh, gw, ntxt, axes):
 
 
 def test_rope_table_vit():
-    c = torch.empty(5 + 32 * 32, 32, device=dev())
+    c = torch.empty(32, 5 + 32 * 32, device=dev())
     s = torch.empty_like(c)
     dit.dit_rope_table_vit(32, 32, 5, 64, 10000.0, c, s)
-    ang = O.rope_angles_vit(32, 32, 5, 64)
-    np.testing.assert_allclose(npf(c), np.cos(ang), atol=2e-6, rtol=0)
-    np.testing.assert_allclose(npf(s), np.sin(ang), atol=2e-6, rtol=0)
+    ang = O.rope_angles_vit(32, 32, 5, 64)   # [n, half]
+    np.testing.assert_allclose(npf(c), np.cos(ang).T, atol=2e-6, rtol=0)
+    np.testing.assert_allclose(npf(s), np.sin(ang).T, atol=2e-6, rtol=0)
 
 
 # ------------------------------------------------------- QKV + attention
@@ -173,8 +173,7 @@ def test_qkv_rope(case):
     n = S * ns
     s_pad = (S + 7) // 8 * 8
     blk = dit.DeviceBlock(dict(w, w_o=w["w_qkv"], w_gu=w["w_qkv"], w_down=w["w_qkv"]), dev())
-    rc = torch.from_numpy(np.cos(ang)).to(dev())
-    rs = torch.from_numpy(np.sin(ang)).to(dev())
+    rc, rs = pair_major_tables(ang)
     qk = torch.zeros(nh + nkv, n, hd, dtype=torch.bfloat16, device=dev())
     vt = torch.zeros(ns, nkv, hd, s_pad, dtype=torch.bfloat16, device=dev())
     dit.dit_qkv_rope(cfg, blk, a.to(dev()), rc, rs, qk, vt, n_seqs=ns)
@@ -326,8 +325,7 @@ def test_qkv_norm_variants(case, kind, order):
     n = S * ns
     s_pad = (S + 7) // 8 * 8
     blk = dit.DeviceBlock(dict(w, w_o=w["w_qkv"], w_gu=w["w_qkv"], w_down=w["w_qkv"]), dev())
-    rc = torch.from_numpy(np.cos(ang)).to(dev())
-    rs = torch.from_numpy(np.sin(ang)).to(dev())
+    rc, rs = pair_major_tables(ang)
     qk = torch.zeros(nh + nkv, n, hd, dtype=torch.bfloat16, device=dev())
     vt = torch.zeros(ns, nkv, hd, s_pad, dtype=torch.bfloat16, device=dev())
     dit.dit_qkv_rope(cfg, blk, a.to(dev()), rc, rs, qk, vt, n_seqs=ns)

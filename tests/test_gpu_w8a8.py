@@ -17,7 +17,7 @@ import torch
 
 from diffusion_transformer_image_gb300 import synth
 from gpu_common import (assert_block_parity, bf16_storage_rows, cosine, dev, max_err_vs_rms, npf,
-                        oracle_angles, oracle_block_config, oracle_weights)
+                        oracle_angles, oracle_block_config, oracle_weights, pair_major_tables)
 from oracle import dit_oracle as O
 from test_gpu_block import (SMALL_BLOCKS, conditioning_pair, run_block_gpu, run_denoise,
                             sample_rows, TINY_DIT)
@@ -248,8 +248,7 @@ def test_qkv_rope_e4m3(case):
     blk = dit.DeviceBlock(dict(w, w_o=w["w_qkv"], w_gu=w["w_qkv"], w_down=w["w_qkv"]), dev(),
                           "w8a8_h256")
     codes, sa = dit.dit_rotate_quantize(a.to(dev()))
-    rc = torch.from_numpy(np.cos(ang)).to(dev())
-    rs = torch.from_numpy(np.sin(ang)).to(dev())
+    rc, rs = pair_major_tables(ang)
     qk = torch.zeros(nh + nkv, n, hd, dtype=torch.bfloat16, device=dev())
     vt = torch.zeros(ns, nkv, hd, s_pad, dtype=torch.bfloat16, device=dev())
     dit.dit_qkv_rope_e4m3(cfg, blk, codes, sa, rc, rs, qk, vt, n_seqs=ns)
