@@ -158,67 +158,26 @@ constexpr bool is_residual() {
   return EPI == EPI_RESIDUAL || EPI == EPI_RESIDUAL_TANH || EPI == EPI_RESIDUAL_SIGMOID;
 }
 
-// Rotates the pairs of one head row by the RoPE table column of its token:
-// pairs (2k, 2k+1) or (k, k + HD/2), angle k.  The tables are pair-major
-// [HD/2][s_len], so the 32 lanes of a warp (32 consecutive tokens) read one
-// pair's entries in one coalesced request.
-template <int HD>
-__device__ __forceinline__ void rope_row(float (&v)[HD], const QkvEpi& q, int row) {
-  const int trow = row % q.s_len;
-  const float* cs = q.rcos + trow;
-  const float* sn = q.rsin + trow;
-  constexpr int KC = 16;  // pairs whose table entries are loaded together
-#pragma unroll
-  for (int k0 = 0; k0 < HD / 2; k0 += KC) {
-    float c[KC], s[KC];
-#pragma unroll
-    for (int e = 0; e < KC; ++e) {
-      c[e] = __ldg(cs + (size_t)(k0 + e) * q.s_len);
-      s[e] = __ldg(sn + (size_t)(k0 + e) * q.s_len);
-    }
-#pragma unroll
-    for (int e = 0; e < KC; ++e) {
-      const int k = k0 + e;
-      if (q.rope_half) {
-        const float a = v[k], bb = v[k + HD / 2];
-        v[k] = a * c[e] - bb * s[e];
-        v[k + HD / 2] = a * s[e] + bb * c[e];
-      } else {
-        const float a = v[2 * k], bb = v[2 * k + 1];
-        v[2 * k] = a * c[e] - bb * s[e];
-        v[2 * k + 1] = a * s[e] + bb * c[e];
-      }
-    }
-  }
+// Loads kept in program order (volatile asm) so that a request stays ahead of
+// the TMEM reads whose latency it is meant to overlap; the tcgen05.ld
+// wrappers are compiler memory barriers, so plain loads would be issued only
+// after them.  The RoPE tables stream through without allocating in L1 (they
+// would evict the gains, biases and column scales that every warp reads).
+__device__ __forceinline__ float ldg_stream(const float* p) {
+  float v;
+  asm volatile("ld.global.nc.L1::no_allocate.f32 %0, [%1];" : "=f"(v) : "l"(p));
+  return v;
+}
+__device__ __forceinline__ float ldg_ordered(const float* p) {
+  float v;
+  asm volatile("ld.global.nc.f32 %0, [%1];" : "=f"(v) : "l"(p));
+  return v;
 }
 
 // The 16 pairs j*16 .. j*16+15 of one head row as two arrays (first and
 // second element of each pair): interleaved pairs (2k, 2k+1) come from the
 // 32 columns from 32 j, rotate-half pairs (k, k + HD/2) from the 16 columns
-// from 16 j and the 16 from HD/2 + 16 j.  pair_cols reads a per-column
-// vector (gains, biases, column scales) the same way.
-template <int HD>
-__device__ __forceinline__ void pair_cols(const float* vec, bool half, int j, float (&a)[16],
-                                          float (&b)[16]) {
-  if (half) {
-    const float4* pa = reinterpret_cast<const float4*>(vec + 16 * j);
-    const float4* pb = reinterpret_cast<const float4*>(vec + HD / 2 + 16 * j);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const float4 x = __ldg(pa + i), y = __ldg(pb + i);
-      a[4 * i] = x.x; a[4 * i + 1] = x.y; a[4 * i + 2] = x.z; a[4 * i + 3] = x.w;
-      b[4 * i] = y.x; b[4 * i + 1] = y.y; b[4 * i + 2] = y.z; b[4 * i + 3] = y.w;
-    }
-  } else {
-    const float4* p4 = reinterpret_cast<const float4*>(vec + 32 * j);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const float4 x = __ldg(p4 + i);
-      a[2 * i] = x.x; b[2 * i] = x.y; a[2 * i + 1] = x.z; b[2 * i + 1] = x.w;
-    }
-  }
-}
-
+// from 16 j and the 16 from HD/2 + 16 j.
 template <int HD>
 __device__ __forceinline__ void tmem_pairs(uint32_t hb, bool half, int j, float (&a)[16],
                                            float (&b)[16]) {
@@ -236,22 +195,52 @@ __device__ __forceinline__ void tmem_pairs(uint32_t hb, bool half, int j, float 
   }
 }
 
-// Rotates pairs 16 j .. 16 j + 15 of the token at table column trow.
-__device__ __forceinline__ void rope_pairs(float (&a)[16], float (&b)[16], const QkvEpi& q,
-                                           int trow, int j) {
-  const float* cs = q.rcos + (size_t)(16 * j) * q.s_len + trow;
-  const float* sn = q.rsin + (size_t)(16 * j) * q.s_len + trow;
-  float c[16], s[16];
+// (x - mean) rstd g + b on the 16 pairs j, the gains and biases read four
+// columns at a time as they are used.
+template <int HD>
+__device__ __forceinline__ void norm_pairs(float (&a)[16], float (&b)[16], const float* g,
+                                           const float* bias, bool half, int j, float mean,
+                                           float rstd) {
+  if (half) {
 #pragma unroll
-  for (int e = 0; e < 16; ++e) {
-    c[e] = __ldg(cs + (size_t)e * q.s_len);
-    s[e] = __ldg(sn + (size_t)e * q.s_len);
+    for (int i = 0; i < 4; ++i) {
+      const float4 ga = __ldg(reinterpret_cast<const float4*>(g + 16 * j) + i);
+      const float4 ba = __ldg(reinterpret_cast<const float4*>(bias + 16 * j) + i);
+      const float4 gb = __ldg(reinterpret_cast<const float4*>(g + HD / 2 + 16 * j) + i);
+      const float4 bb = __ldg(reinterpret_cast<const float4*>(bias + HD / 2 + 16 * j) + i);
+      a[4 * i + 0] = fmaf((a[4 * i + 0] - mean) * rstd, ga.x, ba.x);
+      a[4 * i + 1] = fmaf((a[4 * i + 1] - mean) * rstd, ga.y, ba.y);
+      a[4 * i + 2] = fmaf((a[4 * i + 2] - mean) * rstd, ga.z, ba.z);
+      a[4 * i + 3] = fmaf((a[4 * i + 3] - mean) * rstd, ga.w, ba.w);
+      b[4 * i + 0] = fmaf((b[4 * i + 0] - mean) * rstd, gb.x, bb.x);
+      b[4 * i + 1] = fmaf((b[4 * i + 1] - mean) * rstd, gb.y, bb.y);
+      b[4 * i + 2] = fmaf((b[4 * i + 2] - mean) * rstd, gb.z, bb.z);
+      b[4 * i + 3] = fmaf((b[4 * i + 3] - mean) * rstd, gb.w, bb.w);
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {  // columns 32 j + 4 i .. + 3: pairs 2 i, 2 i + 1
+      const float4 gg = __ldg(reinterpret_cast<const float4*>(g + 32 * j) + i);
+      const float4 bb = __ldg(reinterpret_cast<const float4*>(bias + 32 * j) + i);
+      a[2 * i] = fmaf((a[2 * i] - mean) * rstd, gg.x, bb.x);
+      b[2 * i] = fmaf((b[2 * i] - mean) * rstd, gg.y, bb.y);
+      a[2 * i + 1] = fmaf((a[2 * i + 1] - mean) * rstd, gg.z, bb.z);
+      b[2 * i + 1] = fmaf((b[2 * i + 1] - mean) * rstd, gg.w, bb.w);
+    }
   }
+}
+
+// Rotates pairs 16 j .. 16 j + 15 by this lane's table entries.
+template <int HD>
+__device__ __forceinline__ void rotate_pairs(float (&a)[16], float (&b)[16],
+                                             const float (&tc)[HD / 2], const float (&ts)[HD / 2],
+                                             int j) {
 #pragma unroll
   for (int e = 0; e < 16; ++e) {
+    const float c = tc[16 * j + e], s = ts[16 * j + e];
     const float x = a[e], y = b[e];
-    a[e] = x * c[e] - y * s[e];
-    b[e] = x * s[e] + y * c[e];
+    a[e] = x * c - y * s;
+    b[e] = x * s + y * c;
   }
 }
 
@@ -482,136 +471,146 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const CUtenso
   } else if constexpr (EPI == EPI_QKV) {
     const QkvEpi& q = p.qkv;
     constexpr int HPT = BN / HD;  // heads per tile
+    constexpr int NCH = HD / 32;  // chunks of 32 columns (16 pairs) per head
+    const int trow = row % q.s_len;
+    // this lane's table entries for all HD/2 pairs, the same for every head
+    // of the tile: requested once, before the first head's TMEM passes, so
+    // that their latency overlaps them (tiles of v heads only skip them)
+    float tc[HD / 2], ts[HD / 2];
+    if ((n_blk * BN) / HD < q.nh + q.nkv) {
+#pragma unroll
+      for (int k = 0; k < HD / 2; ++k) {
+        tc[k] = ldg_stream(q.rcos + (size_t)k * q.s_len + trow);
+        ts[k] = ldg_stream(q.rsin + (size_t)k * q.s_len + trow);
+      }
+    }
 #pragma unroll 1
     for (int hh = 0; hh < HPT; ++hh) {
       const int col0 = n_blk * BN + hh * HD;
       if (col0 >= p.N) break;
       const int head = col0 / HD;
       const uint32_t hb = tbase + hh * HD;   // this head's accumulator columns
+      // W8A8: the head's column scales, lane l holding the one of column
+      // 32 c + l (one coalesced load per 32 columns), passed to every lane by
+      // a shuffle where a chunk is scaled
+      float sbl[NCH];
+      if constexpr (F8) {
+#pragma unroll
+        for (int c = 0; c < NCH; ++c) sbl[c] = ldg_ordered(p.sb + col0 + 32 * c + lane);
+      }
+      __syncwarp();
       if (head < q.nh + q.nkv) {
+        if constexpr (F8) {
+          // the row and column scales applied once, in TMEM, so that every
+          // later pass reads scaled values
+#pragma unroll
+          for (int c = 0; c < NCH; ++c) {
+            float x[32];
+            tmem_ld32(hb + 32 * c, x);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) x[i] *= rs * __shfl_sync(0xffffffffu, sbl[c], i);
+            tmem_st32(hb + 32 * c, x);
+          }
+        }
         const bool is_q = head < q.nh;
         const float* g = is_q ? q.qg : q.kg;
         const float* b = is_q ? q.qb : q.kb;
-        const int trow = row % q.s_len;
-        // pass 1: the row's norm statistics over all HD values (of the
-        // rotated row when the rotation comes first), in eight interleaved
-        // partial sums
+        // the norm statistics in one pass over TMEM (of the rotated row when
+        // the rotation comes first): sums of x - x0 and of its squares, x0
+        // the row's first value (a sample of the row, so the variance
+        // formula does not cancel), four partial sums each
         float mean = 0.f, rstd = 1.f;
         if (g != nullptr) {
-          float v[HD];
-          __syncwarp();
+          float s1[4] = {0.f, 0.f, 0.f, 0.f}, s2[4] = {0.f, 0.f, 0.f, 0.f};
+          float x0 = 0.f;
 #pragma unroll
-          for (int c = 0; c < HD / 32; ++c)
-            tmem_ld32(hb + c * 32, *reinterpret_cast<float(*)[32]>(&v[c * 32]));
-          if constexpr (F8) {
+          for (int j = 0; j < NCH; ++j) {
+            float pa[16], pb[16];
+            tmem_pairs<HD>(hb, q.rope_half, j, pa, pb);
+            if (q.rope_first) rotate_pairs<HD>(pa, pb, tc, ts, j);
+            if (j == 0 && !q.rms) x0 = pa[0];
 #pragma unroll
-            for (int c = 0; c < HD / 32; ++c)
-              scale_cols(*reinterpret_cast<float(*)[32]>(&v[c * 32]), rs, p.sb, col0 + c * 32,
-                         p.N);
+            for (int e = 0; e < 16; ++e) {
+              const float da = pa[e] - x0, db = pb[e] - x0;
+              s1[e & 3] += da + db;
+              s2[e & 3] = fmaf(da, da, s2[e & 3]);
+              s2[e & 3] = fmaf(db, db, s2[e & 3]);
+            }
           }
-          if (q.rope_first) rope_row<HD>(v, q, row);
-          if (!q.rms) {
-            float sm[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-            for (int i = 0; i < HD; ++i) sm[i & 7] += v[i];
-            mean = (((sm[0] + sm[1]) + (sm[2] + sm[3])) + ((sm[4] + sm[5]) + (sm[6] + sm[7]))) *
-                   (1.0f / HD);
-          }
-          float ss[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-          for (int i = 0; i < HD; ++i) {
-            const float d = v[i] - mean;
-            ss[i & 7] = fmaf(d, d, ss[i & 7]);
-          }
-          const float var =
-              (((ss[0] + ss[1]) + (ss[2] + ss[3])) + ((ss[4] + ss[5]) + (ss[6] + ss[7]))) *
-              (1.0f / HD);
+          const float m1 = ((s1[0] + s1[1]) + (s1[2] + s1[3])) * (1.0f / HD);
+          const float m2 = ((s2[0] + s2[1]) + (s2[2] + s2[3])) * (1.0f / HD);
+          // RMSNorm: x0 = 0 and no centring, m2 is the mean square
+          mean = q.rms ? 0.0f : x0 + m1;
+          const float var = q.rms ? m2 : fmaxf(m2 - m1 * m1, 0.0f);
           rstd = 1.0f / sqrtf(var + q.eps);
         }
-        // pass 2: 16 pairs at a time from TMEM again: scale, norm and
-        // rotation in the block's order, bf16 into the staging buffers (one
-        // per 64-column box); then one TMA box (64, 32 rows) per 64 columns
-        // of the head-major map [head][token][d].  Rows past M are not
-        // written.
+        // chunk by chunk: norm and rotation in the block's order, bf16 into
+        // the staging buffers (one per 64-column box); then one TMA box
+        // (64, 32 rows) per 64 columns of the head-major map [head][token][d].
+        // Rows past M are not written.
         if (lane == 0) bulk_wait_read<0>();   // both staging buffers free
         __syncwarp();
 #pragma unroll
-        for (int j = 0; j < HD / 32; ++j) {
+        for (int j = 0; j < NCH; ++j) {
           float pa[16], pb[16];
           tmem_pairs<HD>(hb, q.rope_half, j, pa, pb);
-          if constexpr (F8) {
-            float sa[16], sb[16];
-            pair_cols<HD>(p.sb + col0, q.rope_half, j, sa, sb);
-#pragma unroll
-            for (int e = 0; e < 16; ++e) {
-              pa[e] *= rs * sa[e];
-              pb[e] *= rs * sb[e];
-            }
-          }
-          if (q.rope_first) rope_pairs(pa, pb, q, trow, j);
-          if (g != nullptr) {
-            float ga[16], gb[16], ba[16], bb[16];
-            pair_cols<HD>(g, q.rope_half, j, ga, gb);
-            pair_cols<HD>(b, q.rope_half, j, ba, bb);
-#pragma unroll
-            for (int e = 0; e < 16; ++e) {
-              pa[e] = fmaf((pa[e] - mean) * rstd, ga[e], ba[e]);
-              pb[e] = fmaf((pb[e] - mean) * rstd, gb[e], bb[e]);
-            }
-          }
-          if (!q.rope_first) rope_pairs(pa, pb, q, trow, j);
+          if (q.rope_first) rotate_pairs<HD>(pa, pb, tc, ts, j);
+          if (g != nullptr) norm_pairs<HD>(pa, pb, g, b, q.rope_half, j, mean, rstd);
+          if (!q.rope_first) rotate_pairs<HD>(pa, pb, tc, ts, j);
           stage_pairs<HD>(es.buf, lane, q.rope_half, j, pa, pb);
         }
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0 && row0 < p.M) {  // a slab wholly below M stores nothing
 #pragma unroll
-          for (int c = 0; c < HD / 64; ++c) tma_store_3d(tmO, es.buf + c * EBUF_BYTES, c * 64, row0, head);
+          for (int c = 0; c < HD / 64; ++c)
+            tma_store_3d(tmO, es.buf + c * EBUF_BYTES, c * 64, row0, head);
           bulk_commit();
         }
-        es.cur = 0;
       } else {
-        float v[HD];
-        __syncwarp();
-#pragma unroll
-        for (int c = 0; c < HD / 32; ++c)
-          tmem_ld32(hb + c * 32, *reinterpret_cast<float(*)[32]>(&v[c * 32]));
-        if constexpr (F8) {
-#pragma unroll
-          for (int c = 0; c < HD / 32; ++c)
-            scale_cols(*reinterpret_cast<float(*)[32]>(&v[c * 32]), rs, p.sb, col0 + c * 32, p.N);
-        }
+        // v, transposed per sequence.  When the slab's existing rows (< M)
+        // all lie in one sequence and start on a 16-byte boundary of the
+        // transposed row, one TMA box (32 tokens x d channels) from a
+        // transposed staging tile [d][32] that fills both staging buffers of
+        // the warp; otherwise direct stores.
         const int g = head - q.nh - q.nkv;
         const int seq0 = row0 / q.s_len;
         const int j0 = row0 - seq0 * q.s_len;
-        // the slab's existing rows (< M) all in one sequence, starting on a
-        // 16-byte boundary of the transposed row: one TMA box (32 tokens x
-        // d channels) from a transposed staging tile [d][32] filling both
-        // staging buffers of this warp
         const int rows_end = min(row0 + 32, p.M);
-        if (row0 >= p.M) {
-          // a slab wholly below M stores nothing
-        } else if (j0 % 8 == 0 && rows_end <= (seq0 + 1) * q.s_len) {
-          if (lane == 0) bulk_wait_read<0>();   // both staging buffers free
-          __syncwarp();
-          __nv_bfloat16* tb = reinterpret_cast<__nv_bfloat16*>(es.buf);
+        const bool staged = row0 < p.M && j0 % 8 == 0 && rows_end <= (seq0 + 1) * q.s_len;
+        __nv_bfloat16* tb = reinterpret_cast<__nv_bfloat16*>(es.buf);
+        if (staged && lane == 0) bulk_wait_read<0>();   // both staging buffers free
+        __syncwarp();
+        const int seq = row / q.s_len;
+        __nv_bfloat16* dst =
+            q.vt + ((size_t)(seq * q.nkv + g) * HD) * q.s_pad + (row - seq * q.s_len);
 #pragma unroll
-          for (int c = 0; c < HD; ++c) tb[c * 32 + lane] = __float2bfloat16_rn(v[c]);
+        for (int c = 0; c < NCH; ++c) {
+          float x[32];
+          tmem_ld32(hb + c * 32, x);
+          if constexpr (F8) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) x[i] *= rs * __shfl_sync(0xffffffffu, sbl[c], i);
+          }
+          if (staged) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) tb[(c * 32 + i) * 32 + lane] = __float2bfloat16_rn(x[i]);
+          } else if (row_ok) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              dst[(size_t)(c * 32 + i) * q.s_pad] = __float2bfloat16_rn(x[i]);
+          }
+        }
+        if (staged) {
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
             tma_store_2d(tmV, tb, j0, (seq0 * q.nkv + g) * HD);
             bulk_commit();
           }
-          es.cur = 0;   // every staged write of this epilogue first waits for both buffers
-        } else if (row_ok) {
-          const int seq = row / q.s_len;
-          const int j = row - seq * q.s_len;
-          __nv_bfloat16* dst = q.vt + ((size_t)(seq * q.nkv + g) * HD) * q.s_pad + j;
-#pragma unroll
-          for (int c = 0; c < HD; ++c) dst[(size_t)c * q.s_pad] = __float2bfloat16_rn(v[c]);
         }
       }
+      es.cur = 0;   // every staged write of this epilogue first waits for both buffers
     }
   }
 }
