@@ -195,52 +195,87 @@ __device__ __forceinline__ void tmem_pairs(uint32_t hb, bool half, int j, float 
   }
 }
 
-// (x - mean) rstd g + b on the 16 pairs j, the gains and biases read four
-// columns at a time as they are used.
+// The arithmetic below runs on f32x2 operands over two neighbouring pairs:
+// A = (a[e], a[e+1]) and B = (b[e], b[e+1]), e even, half the instructions
+// of the scalar form.
+__device__ __forceinline__ float2 f2(float x, float y) { return make_float2(x, y); }
+
+// Shifted sums of the 16 pairs j for the norm statistics: s1 += x - x0,
+// s2 += (x - x0)^2 (x0 broadcast in nx0 as -x0).
+__device__ __forceinline__ void stat_pairs(const float (&a)[16], const float (&b)[16], float2 nx0,
+                                           float2 (&s1)[2], float2 (&s2)[2]) {
+#pragma unroll
+  for (int e = 0; e < 16; e += 2) {
+    const float2 da = __fadd2_rn(f2(a[e], a[e + 1]), nx0);
+    const float2 db = __fadd2_rn(f2(b[e], b[e + 1]), nx0);
+    s1[0] = __fadd2_rn(s1[0], da);
+    s1[1] = __fadd2_rn(s1[1], db);
+    s2[0] = __ffma2_rn(da, da, s2[0]);
+    s2[1] = __ffma2_rn(db, db, s2[1]);
+  }
+}
+
+// x rstd - mean rstd, then times g plus b, on the 16 pairs j; the gains and
+// biases read four columns at a time as they are used.
 template <int HD>
 __device__ __forceinline__ void norm_pairs(float (&a)[16], float (&b)[16], const float* g,
                                            const float* bias, bool half, int j, float mean,
                                            float rstd) {
+  const float2 r2 = f2(rstd, rstd);
+  const float2 o2 = f2(-mean * rstd, -mean * rstd);
   if (half) {
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
+    for (int i = 0; i < 4; ++i) {  // pairs 4 i .. 4 i + 3: columns 16 j + 4 i and HD/2 + 16 j + 4 i
       const float4 ga = __ldg(reinterpret_cast<const float4*>(g + 16 * j) + i);
       const float4 ba = __ldg(reinterpret_cast<const float4*>(bias + 16 * j) + i);
       const float4 gb = __ldg(reinterpret_cast<const float4*>(g + HD / 2 + 16 * j) + i);
       const float4 bb = __ldg(reinterpret_cast<const float4*>(bias + HD / 2 + 16 * j) + i);
-      a[4 * i + 0] = fmaf((a[4 * i + 0] - mean) * rstd, ga.x, ba.x);
-      a[4 * i + 1] = fmaf((a[4 * i + 1] - mean) * rstd, ga.y, ba.y);
-      a[4 * i + 2] = fmaf((a[4 * i + 2] - mean) * rstd, ga.z, ba.z);
-      a[4 * i + 3] = fmaf((a[4 * i + 3] - mean) * rstd, ga.w, ba.w);
-      b[4 * i + 0] = fmaf((b[4 * i + 0] - mean) * rstd, gb.x, bb.x);
-      b[4 * i + 1] = fmaf((b[4 * i + 1] - mean) * rstd, gb.y, bb.y);
-      b[4 * i + 2] = fmaf((b[4 * i + 2] - mean) * rstd, gb.z, bb.z);
-      b[4 * i + 3] = fmaf((b[4 * i + 3] - mean) * rstd, gb.w, bb.w);
+      float2 x = __ffma2_rn(f2(a[4 * i], a[4 * i + 1]), r2, o2);
+      x = __ffma2_rn(x, f2(ga.x, ga.y), f2(ba.x, ba.y));
+      a[4 * i] = x.x;
+      a[4 * i + 1] = x.y;
+      x = __ffma2_rn(f2(a[4 * i + 2], a[4 * i + 3]), r2, o2);
+      x = __ffma2_rn(x, f2(ga.z, ga.w), f2(ba.z, ba.w));
+      a[4 * i + 2] = x.x;
+      a[4 * i + 3] = x.y;
+      x = __ffma2_rn(f2(b[4 * i], b[4 * i + 1]), r2, o2);
+      x = __ffma2_rn(x, f2(gb.x, gb.y), f2(bb.x, bb.y));
+      b[4 * i] = x.x;
+      b[4 * i + 1] = x.y;
+      x = __ffma2_rn(f2(b[4 * i + 2], b[4 * i + 3]), r2, o2);
+      x = __ffma2_rn(x, f2(gb.z, gb.w), f2(bb.z, bb.w));
+      b[4 * i + 2] = x.x;
+      b[4 * i + 3] = x.y;
     }
   } else {
 #pragma unroll
     for (int i = 0; i < 8; ++i) {  // columns 32 j + 4 i .. + 3: pairs 2 i, 2 i + 1
       const float4 gg = __ldg(reinterpret_cast<const float4*>(g + 32 * j) + i);
       const float4 bb = __ldg(reinterpret_cast<const float4*>(bias + 32 * j) + i);
-      a[2 * i] = fmaf((a[2 * i] - mean) * rstd, gg.x, bb.x);
-      b[2 * i] = fmaf((b[2 * i] - mean) * rstd, gg.y, bb.y);
-      a[2 * i + 1] = fmaf((a[2 * i + 1] - mean) * rstd, gg.z, bb.z);
-      b[2 * i + 1] = fmaf((b[2 * i + 1] - mean) * rstd, gg.w, bb.w);
+      float2 x = __ffma2_rn(f2(a[2 * i], a[2 * i + 1]), r2, o2);
+      x = __ffma2_rn(x, f2(gg.x, gg.z), f2(bb.x, bb.z));
+      a[2 * i] = x.x;
+      a[2 * i + 1] = x.y;
+      x = __ffma2_rn(f2(b[2 * i], b[2 * i + 1]), r2, o2);
+      x = __ffma2_rn(x, f2(gg.y, gg.w), f2(bb.y, bb.w));
+      b[2 * i] = x.x;
+      b[2 * i + 1] = x.y;
     }
   }
 }
 
-// Rotates pairs 16 j .. 16 j + 15 by this lane's table entries.
+// Rotates pairs 16 j .. 16 j + 15 by this lane's table entries:
+// a' = a c - b s, b' = a s + b c.
 template <int HD>
 __device__ __forceinline__ void rotate_pairs(float (&a)[16], float (&b)[16],
                                              const float (&tc)[HD / 2], const float (&ts)[HD / 2],
                                              int j) {
 #pragma unroll
   for (int e = 0; e < 16; ++e) {
-    const float c = tc[16 * j + e], s = ts[16 * j + e];
+    const float c = tc[16 * j + e], sn = ts[16 * j + e];
     const float x = a[e], y = b[e];
-    a[e] = x * c - y * s;
-    b[e] = x * s + y * c;
+    a[e] = x * c - y * sn;
+    b[e] = x * sn + y * c;
   }
 }
 
@@ -521,7 +556,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const CUtenso
         // formula does not cancel), four partial sums each
         float mean = 0.f, rstd = 1.f;
         if (g != nullptr) {
-          float s1[4] = {0.f, 0.f, 0.f, 0.f}, s2[4] = {0.f, 0.f, 0.f, 0.f};
+          float2 s1[2] = {f2(0.f, 0.f), f2(0.f, 0.f)}, s2[2] = {f2(0.f, 0.f), f2(0.f, 0.f)};
           float x0 = 0.f;
 #pragma unroll
           for (int j = 0; j < NCH; ++j) {
@@ -529,16 +564,10 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const CUtenso
             tmem_pairs<HD>(hb, q.rope_half, j, pa, pb);
             if (q.rope_first) rotate_pairs<HD>(pa, pb, tc, ts, j);
             if (j == 0 && !q.rms) x0 = pa[0];
-#pragma unroll
-            for (int e = 0; e < 16; ++e) {
-              const float da = pa[e] - x0, db = pb[e] - x0;
-              s1[e & 3] += da + db;
-              s2[e & 3] = fmaf(da, da, s2[e & 3]);
-              s2[e & 3] = fmaf(db, db, s2[e & 3]);
-            }
+            stat_pairs(pa, pb, f2(-x0, -x0), s1, s2);
           }
-          const float m1 = ((s1[0] + s1[1]) + (s1[2] + s1[3])) * (1.0f / HD);
-          const float m2 = ((s2[0] + s2[1]) + (s2[2] + s2[3])) * (1.0f / HD);
+          const float m1 = ((s1[0].x + s1[0].y) + (s1[1].x + s1[1].y)) * (1.0f / HD);
+          const float m2 = ((s2[0].x + s2[0].y) + (s2[1].x + s2[1].y)) * (1.0f / HD);
           // RMSNorm: x0 = 0 and no centring, m2 is the mean square
           mean = q.rms ? 0.0f : x0 + m1;
           const float var = q.rms ? m2 : fmaxf(m2 - m1 * m1, 0.0f);
