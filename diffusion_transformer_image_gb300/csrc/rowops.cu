@@ -110,6 +110,81 @@ __global__ void __launch_bounds__(LN_THREADS) ln_modulate_kernel(
   }
 }
 
+// One warp per row for narrow rows, H = 128 NV (H <= 1024): the row in 32
+// lanes x NV float4, sums by shuffles only (no block barrier), the
+// modulation vectors read as they are used.  Rows are independent warps, so
+// an SM keeps dozens of rows in flight and none waits on another's
+// reduction.  (A 4096-wide row would take 128 registers per lane and fewer
+// rows per SM: the block kernel above is faster there.)
+constexpr int LNW_WARPS = 4;
+
+__device__ __forceinline__ float warp_allsum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+template <int MODE, bool RMS, int NV>
+__global__ void __launch_bounds__(LNW_WARPS * 32) ln_modulate_warp_kernel(
+    const float* __restrict__ x, long long ldx, int rows, const float* __restrict__ p0,
+    const float* __restrict__ p1, float eps, __nv_bfloat16* __restrict__ out, long long ldo,
+    __nv_bfloat16* __restrict__ out_lo) {
+  constexpr int H = 128 * NV;
+  const int row = blockIdx.x * LNW_WARPS + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= rows) return;
+  const float4* xr = reinterpret_cast<const float4*>(x + (size_t)row * ldx);
+  float4 v[NV];
+#pragma unroll
+  for (int i = 0; i < NV; ++i) v[i] = __ldg(xr + lane + 32 * i);
+  float s = 0.f;
+#pragma unroll
+  for (int i = 0; i < NV; ++i) s += (v[i].x + v[i].y) + (v[i].z + v[i].w);
+  // RMSNorm keeps the mean (it divides by the root mean square instead)
+  const float mean = RMS ? 0.0f : warp_allsum(s) * (1.0f / H);
+  float ss = 0.f;
+#pragma unroll
+  for (int i = 0; i < NV; ++i) {
+    v[i].x -= mean; v[i].y -= mean; v[i].z -= mean; v[i].w -= mean;
+    ss += (v[i].x * v[i].x + v[i].y * v[i].y) + (v[i].z * v[i].z + v[i].w * v[i].w);
+  }
+  const float rstd = 1.0f / sqrtf(warp_allsum(ss) * (1.0f / H) + eps);
+  uint2* orow = reinterpret_cast<uint2*>(out + (size_t)row * ldo);
+  const float4* a4 = reinterpret_cast<const float4*>(p0);
+  const float4* b4 = reinterpret_cast<const float4*>(p1);
+#pragma unroll
+  for (int i = 0; i < NV; ++i) {
+    const int idx = lane + 32 * i;
+    const float4 a = __ldg(a4 + idx), b = __ldg(b4 + idx);
+    float4 n = v[i];
+    n.x *= rstd; n.y *= rstd; n.z *= rstd; n.w *= rstd;
+    float4 r;
+    if (MODE == 0) {  // AdaLN: a = shift, b = scale
+      r.x = fmaf(n.x, 1.0f + b.x, a.x);
+      r.y = fmaf(n.y, 1.0f + b.y, a.y);
+      r.z = fmaf(n.z, 1.0f + b.z, a.z);
+      r.w = fmaf(n.w, 1.0f + b.w, a.w);
+    } else {          // affine: a = gain, b = bias
+      r.x = fmaf(n.x, a.x, b.x);
+      r.y = fmaf(n.y, a.y, b.y);
+      r.z = fmaf(n.z, a.z, b.z);
+      r.w = fmaf(n.w, a.w, b.w);
+    }
+    uint2 u;
+    u.x = pack_bf16x2(r.x, r.y);
+    u.y = pack_bf16x2(r.z, r.w);
+    orow[idx] = u;
+    if (out_lo) {
+      const __nv_bfloat162* hv = reinterpret_cast<const __nv_bfloat162*>(&u);
+      const float2 h0 = __bfloat1622float2(hv[0]), h1 = __bfloat1622float2(hv[1]);
+      uint2 l;
+      l.x = pack_bf16x2(r.x - h0.x, r.y - h0.y);
+      l.y = pack_bf16x2(r.z - h1.x, r.w - h1.y);
+      reinterpret_cast<uint2*>(out_lo + (size_t)row * ldo)[idx] = l;
+    }
+  }
+}
+
 // ------------------------------------------------------------------- Euler
 // x <- x + (sigma_next - sigma) v, the product rounded before the add
 // ([ZFLOW] section IV, Euler sign +1).
@@ -326,6 +401,25 @@ cudaError_t launch_ln_modulate(int mode, const float* x, long long ldx, int rows
   if (H > LN_THREADS * 4 * LN_MAXV || (H & 3)) return cudaErrorInvalidValue;
   const int grid = rows;
   if (grid == 0) return cudaSuccess;
+  // widths the warp-per-row kernel is built for
+  if (H == 1024 || H == 256) {
+    const int g = (rows + LNW_WARPS - 1) / LNW_WARPS;
+#define DIT_LNW(M, R, NV)                                                                \
+  ln_modulate_warp_kernel<M, R, NV><<<g, LNW_WARPS * 32, 0, st>>>(x, ldx, rows, p0, p1, eps, out, \
+                                                                  ldo, out_lo)
+#define DIT_LNW_H(M, R) (H == 1024 ? DIT_LNW(M, R, 8) : DIT_LNW(M, R, 2))
+    switch (mode) {
+      case 0: DIT_LNW_H(0, false); break;
+      case 1: DIT_LNW_H(1, false); break;
+      case 2: DIT_LNW_H(0, true); break;
+      case 3: DIT_LNW_H(1, true); break;
+      default: return cudaErrorInvalidValue;
+    }
+#undef DIT_LNW_H
+#undef DIT_LNW
+    count_launch();
+    return cudaGetLastError();
+  }
   const bool small = H <= LN_THREADS * 4 * 4;
 #define DIT_LN_LAUNCH(M, R)                                                                     \
   (small ? (ln_modulate_kernel<M, R, 4><<<grid, LN_THREADS, 0, st>>>(x, ldx, rows, H, p0, p1, eps, \
