@@ -51,6 +51,9 @@ def parse():
                    help="skip the W8A8-format step and block measurements")
     p.add_argument("--no-secondary", action="store_true",
                    help="skip the Krea-shaped step and the ViT backbone measurements")
+    p.add_argument("--no-breakdown", action="store_true",
+                   help="skip the per-kernel breakdown and the library bars timed before the "
+                        "steps, so that an ncu launch list can skip exactly the warm-up steps")
     return p.parse_args()
 
 
@@ -546,6 +549,95 @@ def run_ours(args, rank, world, local):
         dit.dit_denoise_step(cfg, model, latent, text, wl.grid_h, wl.grid_w, sig[j], sig[j + 1],
                              ws=ws)
 
+    per_block, step_flops = workload_flops(wl, wl.n_layers)
+
+    # ---- per-kernel breakdown and the dominant kernel's roofline, timed
+    # first as a short burst (a few repetitions of one block's stages), the
+    # regime of the burst peak they are held to; the library bars on the
+    # same shapes right after, in the same regime
+    mod = torch.empty(6, wl.hidden, device=dev)
+    fin = torch.empty(2, wl.hidden, device=dev)
+    scratch = torch.empty(wl.t_dim + 2 * wl.hidden, device=dev)
+    dit.dit_timestep_conditioning(cfg, model, sig[0], mod, fin, scratch)
+    rc = torch.empty(wl.head_dim // 2, wl.n_tokens, device=dev)
+    rs = torch.empty_like(rc)
+    dit.dit_rope_table_grid(wl.grid_h, wl.grid_w, wl.n_txt, wl.rope_axes, wl.rope_theta, rc, rs)
+    x = torch.randn(wl.n_tokens, wl.hidden, device=dev)
+    peaks, peak_src = load_peaks()
+    # Kernels timed alone (a few repetitions of one block's stages) are held
+    # to the burst bf16 peak; the whole step, seconds of back-to-back work
+    # under the power cap, to the sustained one.
+    tc_peak = peak_value(peaks, "bf16_tflops")
+    tc_sustained = peak_value(peaks, "bf16_tflops_sustained")
+    hbm_peak = peak_value(peaks, "hbm_gbs")
+
+    def time_ms(f, reps=10):
+        f()
+        torch.cuda.synchronize()
+        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a0.record(stream)
+        for _ in range(reps):
+            f()
+        a1.record(stream)
+        torch.cuda.synchronize()
+        return a0.elapsed_time(a1) / reps
+
+    kernels, roof, bars, st8, kclk = None, None, None, None, None
+    if not args.no_breakdown:
+        kclocks = ClockSampler(local)
+        if rank == 0:
+            kclocks.start()
+            time.sleep(0.3)
+        stages = stage_breakdown(dit, wl, model, x, mod, rc, rs)
+        kernels = kernel_table(stages, per_block, wl, tc_peak, hbm_peak)
+        dom = max((k for k in kernels if k != "ln_modulate"),
+                  key=lambda k: kernels[k]["ms_per_block"])
+        roof = {"kernel": dom, "bound": "tensor", "achieved": kernels[dom]["achieved"],
+                "peak": tc_peak, "unit": "TFLOP/s", "frac": kernels[dom]["frac"],
+                "traffic": kernels[dom]["traffic"],
+                "peak_source": f"{peak_src} bf16_tflops (burst: the kernel is timed alone)",
+                "algorithmic": f"{per_block[dom]:.4e} FLOP per launch"}
+        # Library bars on the block's shapes, for context only (the product path
+        # never calls them): cuBLAS through torch.matmul for each projection
+        # without its fused tail, and torch's fused scaled-dot-product attention
+        # (backend of torch's choosing) for the joint attention.
+        bars = {"note": "torch.matmul (cuBLAS) and torch scaled_dot_product_attention on the "
+                        "same shapes; context only, not on the product path"}
+        try:
+            n, H, F = wl.n_tokens, wl.hidden, wl.ffn
+            nh, nkv, d = wl.n_heads, wl.n_kv_heads, wl.head_dim
+            g = torch.Generator(device=dev)
+            g.manual_seed(7)
+            for name, (kin, kout) in (("qkv", (H, (nh + 2 * nkv) * d)), ("out", (nh * d, H)),
+                                      ("gate_up", (H, 2 * F)), ("down", (F, H))):
+                a_l = torch.randn(n, kin, device=dev, generator=g).to(torch.bfloat16)
+                w_l = (0.02 * torch.randn(kout, kin, device=dev, generator=g)).to(torch.bfloat16)
+                ms_l = time_ms(lambda: torch.matmul(a_l, w_l.t()))
+                tf = per_block[name] / (ms_l * 1e-3) / 1e12
+                bars[name] = {"ms": round(ms_l, 4), "achieved": round(tf, 1), "unit": "TFLOP/s",
+                              "frac": round(tf / tc_peak, 3)}
+                del a_l, w_l
+            q_l = torch.randn(1, nh, n, d, device=dev, generator=g).to(torch.bfloat16)
+            k_l = torch.randn(1, nkv, n, d, device=dev, generator=g).to(torch.bfloat16)
+            v_l = torch.randn(1, nkv, n, d, device=dev, generator=g).to(torch.bfloat16)
+            if nkv != nh:
+                k_l = k_l.repeat_interleave(nh // nkv, dim=1)
+                v_l = v_l.repeat_interleave(nh // nkv, dim=1)
+            sdpa = torch.nn.functional.scaled_dot_product_attention
+            ms_l = time_ms(lambda: sdpa(q_l, k_l, v_l))
+            tf = per_block["attention"] / (ms_l * 1e-3) / 1e12
+            bars["attention"] = {"ms": round(ms_l, 4), "achieved": round(tf, 1), "unit": "TFLOP/s",
+                                 "frac": round(tf / tc_peak, 3)}
+            del q_l, k_l, v_l
+        except Exception as exc:  # the bars are context: never let them cost the line
+            bars["error"] = f"{type(exc).__name__}: {exc}"[:200]
+        if not args.no_w8a8:
+            blk8_0 = dit.DeviceBlock(dict(model.blocks[0].t), dev, "w8a8_h256")
+            st8 = stage_breakdown_w8a8(dit, wl, blk8_0, x, mod, rc, rs)
+            del blk8_0
+        kclk = kclocks.stop() if rank == 0 else None
+
+    # ---- the headline: `steps` whole denoise steps back to back
     for i in range(args.warmup):
         step(i)
     torch.cuda.synchronize()
@@ -573,7 +665,6 @@ def run_ours(args, rank, world, local):
         raise RuntimeError(f"device error word set during the bench: {status}")
     elapsed_ms = max_over_ranks(elapsed_ms, world, dev)
     value, ms_per_step_rank = replica_metrics(elapsed_ms, args.steps, world)
-    per_block, step_flops = workload_flops(wl, wl.n_layers)
     tflops = step_flops / (ms_per_step_rank * 1e-3) / 1e12
 
     # ---- the 8-step loop captured once as a CUDA graph and replayed (the
@@ -611,59 +702,34 @@ def run_ours(args, rank, world, local):
     lat_dev = torch.empty_like(latent0)
     txt_dev = torch.empty_like(text)
 
+    # Each step also records CUDA events around its device work, so that the
+    # host's share (copies' latency, launch, synchronisation) is separated
+    # from clock drift between this loop and the timed one above.
+    e2e_dev = []
+
     def e2e_step(i):
         j = i % 8
         lat_dev.copy_(lat_host, non_blocking=True)
         txt_dev.copy_(txt_host, non_blocking=True)
+        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a0.record(stream)
         dit.dit_denoise_step(cfg, model, lat_dev, txt_dev, wl.grid_h, wl.grid_w, sig[j],
                              sig[j + 1], ws=ws)
+        a1.record(stream)
         out_host.copy_(lat_dev, non_blocking=True)
         stream.synchronize()
+        e2e_dev.append(a0.elapsed_time(a1))
 
     for i in range(max(3, args.warmup)):
         e2e_step(i)
+    e2e_dev.clear()
     t0 = time.perf_counter()
     for i in range(args.steps):
         e2e_step(i)
     e2e_ms = (time.perf_counter() - t0) * 1e3 / args.steps
+    e2e_dev_ms = sum(e2e_dev) / len(e2e_dev)
     h2d = lat_host.numel() * 4 + txt_host.numel() * 2
     d2h = out_host.numel() * 4
-
-    # ---- per-kernel breakdown and the dominant kernel's roofline
-    mod = torch.empty(6, wl.hidden, device=dev)
-    fin = torch.empty(2, wl.hidden, device=dev)
-    scratch = torch.empty(wl.t_dim + 2 * wl.hidden, device=dev)
-    dit.dit_timestep_conditioning(cfg, model, sig[0], mod, fin, scratch)
-    rc = torch.empty(wl.head_dim // 2, wl.n_tokens, device=dev)
-    rs = torch.empty_like(rc)
-    dit.dit_rope_table_grid(wl.grid_h, wl.grid_w, wl.n_txt, wl.rope_axes, wl.rope_theta, rc, rs)
-    x = torch.randn(wl.n_tokens, wl.hidden, device=dev)
-    stages = stage_breakdown(dit, wl, model, x, mod, rc, rs)
-    peaks, peak_src = load_peaks()
-    # Kernels timed alone (a few repetitions of one block's stages) are held
-    # to the burst bf16 peak; the whole step, seconds of back-to-back work
-    # under the power cap, to the sustained one.
-    tc_peak = peak_value(peaks, "bf16_tflops")
-    tc_sustained = peak_value(peaks, "bf16_tflops_sustained")
-    hbm_peak = peak_value(peaks, "hbm_gbs")
-    kernels = kernel_table(stages, per_block, wl, tc_peak, hbm_peak)
-    dom = max((k for k in kernels if k != "ln_modulate"), key=lambda k: kernels[k]["ms_per_block"])
-    roof = {"kernel": dom, "bound": "tensor", "achieved": kernels[dom]["achieved"],
-            "peak": tc_peak, "unit": "TFLOP/s", "frac": kernels[dom]["frac"],
-            "traffic": kernels[dom]["traffic"],
-            "peak_source": f"{peak_src} bf16_tflops (burst: the kernel is timed alone)",
-            "algorithmic": f"{per_block[dom]:.4e} FLOP per launch"}
-
-    def time_ms(f, reps=10):
-        f()
-        torch.cuda.synchronize()
-        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a0.record(stream)
-        for _ in range(reps):
-            f()
-        a1.record(stream)
-        torch.cuda.synchronize()
-        return a0.elapsed_time(a1) / reps
 
     # Whole-block time of the workload's block and of the variant the ERNIE
     # page draws (RMSNorm, RoPE then qk-norm, clamped tanh-GELU GLU), same
@@ -680,41 +746,6 @@ def run_ours(args, rank, world, local):
         variants[vname] = {"ms_per_block": round(ms_v, 4),
                            "tflops": round(sum(per_block.values()) / (ms_v * 1e-3) / 1e12, 1)}
     del bws
-
-    # Library bars on the block's shapes, for context only (the product path
-    # never calls them): cuBLAS through torch.matmul for each projection
-    # without its fused tail, and torch's fused scaled-dot-product attention
-    # (backend of torch's choosing) for the joint attention.
-    bars = {"note": "torch.matmul (cuBLAS) and torch scaled_dot_product_attention on the "
-                    "same shapes; context only, not on the product path"}
-    try:
-        n, H, F = wl.n_tokens, wl.hidden, wl.ffn
-        nh, nkv, d = wl.n_heads, wl.n_kv_heads, wl.head_dim
-        g = torch.Generator(device=dev)
-        g.manual_seed(7)
-        for name, (kin, kout) in (("qkv", (H, (nh + 2 * nkv) * d)), ("out", (nh * d, H)),
-                                  ("gate_up", (H, 2 * F)), ("down", (F, H))):
-            a_l = torch.randn(n, kin, device=dev, generator=g).to(torch.bfloat16)
-            w_l = (0.02 * torch.randn(kout, kin, device=dev, generator=g)).to(torch.bfloat16)
-            ms_l = time_ms(lambda: torch.matmul(a_l, w_l.t()))
-            tf = per_block[name] / (ms_l * 1e-3) / 1e12
-            bars[name] = {"ms": round(ms_l, 4), "achieved": round(tf, 1), "unit": "TFLOP/s",
-                          "frac": round(tf / tc_peak, 3)}
-            del a_l, w_l
-        q_l = torch.randn(1, nh, n, d, device=dev, generator=g).to(torch.bfloat16)
-        k_l = torch.randn(1, nkv, n, d, device=dev, generator=g).to(torch.bfloat16)
-        v_l = torch.randn(1, nkv, n, d, device=dev, generator=g).to(torch.bfloat16)
-        if nkv != nh:
-            k_l = k_l.repeat_interleave(nh // nkv, dim=1)
-            v_l = v_l.repeat_interleave(nh // nkv, dim=1)
-        sdpa = torch.nn.functional.scaled_dot_product_attention
-        ms_l = time_ms(lambda: sdpa(q_l, k_l, v_l))
-        tf = per_block["attention"] / (ms_l * 1e-3) / 1e12
-        bars["attention"] = {"ms": round(ms_l, 4), "achieved": round(tf, 1), "unit": "TFLOP/s",
-                             "frac": round(tf / tc_peak, 3)}
-        del q_l, k_l, v_l
-    except Exception as exc:  # the bars are context: never let them cost the line
-        bars["error"] = f"{type(exc).__name__}: {exc}"[:200]
 
     # HBM-bound kernels on buffers far larger than L2 (their per-block sizes
     # above are partly L2-resident and launch-bound): LayerNorm + modulate
@@ -772,30 +803,31 @@ def run_ours(args, rank, world, local):
             raise RuntimeError("device error word set during the W8A8 steps")
         ms8 = w0.elapsed_time(w1) / args.steps
         fp8_peak = 2.0 * tc_peak   # kernels timed alone: twice the burst bf16 peak
-        st8 = stage_breakdown_w8a8(dit, wl, blocks8[0], x, mod, rc, rs)
-        k8 = {}
-        n_el = wl.n_tokens
-        bytes_rq = {"ln_rotate_quantize": 2 * 5.0 * n_el * wl.hidden,    # two launches
-                    "rotate_quantize_o": 3.0 * n_el * wl.n_heads * wl.head_dim,
-                    "rotate_quantize_h": 3.0 * n_el * wl.ffn}
-        traffic8 = {"ln_rotate_quantize": "ln_rotate_quantize", "qkv": "f8_qkv",
-                    "attention": "attention", "rotate_quantize_o": "rotate_quantize_o",
-                    "out": "f8_out", "gate_up": "f8_gate_up",
-                    "rotate_quantize_h": "rotate_quantize_h", "down": "f8_down"}
-        for name, ms in st8.items():
-            if name in bytes_rq:
-                gbs = bytes_rq[name] / (ms * 1e-3) / 1e9
-                k8[name] = {"ms_per_block": round(ms, 4), "bound": "hbm",
-                            "achieved": round(gbs, 1), "unit": "GB/s",
-                            "frac": round(gbs / hbm_peak, 3)}
-            else:
-                tf = per_block[name] / (ms * 1e-3) / 1e12
-                pk = tc_peak if name == "attention" else fp8_peak
-                k8[name] = {"ms_per_block": round(ms, 4), "bound": "tensor",
-                            "achieved": round(tf, 1), "unit": "TFLOP/s",
-                            "frac": round(tf / pk, 3),
-                            "dtype": "bf16" if name == "attention" else "e4m3"}
-            k8[name]["traffic"] = traffic_for(traffic8[name])
+        k8 = None
+        if st8 is not None:
+            k8 = {}
+            n_el = wl.n_tokens
+            bytes_rq = {"ln_rotate_quantize": 2 * 5.0 * n_el * wl.hidden,    # two launches
+                        "rotate_quantize_o": 3.0 * n_el * wl.n_heads * wl.head_dim,
+                        "rotate_quantize_h": 3.0 * n_el * wl.ffn}
+            traffic8 = {"ln_rotate_quantize": "ln_rotate_quantize", "qkv": "f8_qkv",
+                        "attention": "attention", "rotate_quantize_o": "rotate_quantize_o",
+                        "out": "f8_out", "gate_up": "f8_gate_up",
+                        "rotate_quantize_h": "rotate_quantize_h", "down": "f8_down"}
+            for name, ms in st8.items():
+                if name in bytes_rq:
+                    gbs = bytes_rq[name] / (ms * 1e-3) / 1e9
+                    k8[name] = {"ms_per_block": round(ms, 4), "bound": "hbm",
+                                "achieved": round(gbs, 1), "unit": "GB/s",
+                                "frac": round(gbs / hbm_peak, 3)}
+                else:
+                    tf = per_block[name] / (ms * 1e-3) / 1e12
+                    pk = tc_peak if name == "attention" else fp8_peak
+                    k8[name] = {"ms_per_block": round(ms, 4), "bound": "tensor",
+                                "achieved": round(tf, 1), "unit": "TFLOP/s",
+                                "frac": round(tf / pk, 3),
+                                "dtype": "bf16" if name == "attention" else "e4m3"}
+                k8[name]["traffic"] = traffic_for(traffic8[name])
         bws8 = dit.workspace(dit.dit_block_workspace_bytes(cfg8.block, wl.n_tokens), dev)
         xv = x.clone()
         ms_b8 = time_ms(lambda: dit.dit_block_forward(cfg8.block, blocks8[0], xv, mod, rc, rs,
@@ -836,12 +868,15 @@ def run_ours(args, rank, world, local):
                               f"back to back under the power cap)",
             "clocks": clk,
             "e2e": {"value": round(e2e_ms, 4), "unit": UNIT, "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h},
+                    "d2h_bytes_per_step": d2h,
+                    "device_ms_per_step": round(e2e_dev_ms, 4),
+                    "host_ms_per_step": round(e2e_ms - e2e_dev_ms, 4)},
             "gpu_launches": launches,
             "graph_replay_ms_per_step": graph_ms if not isinstance(graph_ms, float)
             else round(graph_ms, 4),
             "roofline": roof,
             "kernels": kernels,
+            "kernels_clocks": kclk,
             "hbm_kernels_large": hbm,
             "block_variants": variants,
             "library_bars": bars,
