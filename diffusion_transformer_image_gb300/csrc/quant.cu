@@ -205,9 +205,14 @@ __global__ void __launch_bounds__(RQ_THREADS) ln_rotq_kernel(
 }
 
 // ------------------------------------------------------------ TMA-ring kernels
-constexpr int RQT_STAGES = 4;
 constexpr int RQT_MAX_THREADS = 512;     // K <= 16384
 constexpr int RQT_LN_MAX_THREADS = 256;  // H <= 8192
+// Rows in flight per CTA.  A CTA codes its rows one after another behind
+// block barriers, so the kernels are bound by that chain's latency unless
+// many CTAs share an SM: a two-row ring keeps the shared memory per CTA
+// small (for 4096-wide rows 9 bf16 or 4 fp32 CTAs per SM, then limited by
+// registers), and 2 x (CTAs per SM) rows are still in flight per SM.
+constexpr int RQT_STAGES = 2;
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
   return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) &
@@ -391,7 +396,8 @@ __global__ void __launch_bounds__(RQT_LN_MAX_THREADS) ln_rotq_tma_kernel(
       rqt_issue(smem, row_bytes, full, s, &tm, blockIdx.x + s * G);
   }
   // this thread's modulation parameters (32 consecutive columns), kept in
-  // registers for every row
+  // registers for every row (read per row they would come from L2: the L1
+  // left beside the CTAs' rings is smaller than the two vectors)
   float pa[32], pb[32];
   {
     const float4* a4 = reinterpret_cast<const float4*>(p0 + (size_t)t * 32);
