@@ -130,32 +130,28 @@ def test_block_variants_small(name, variant):
     assert_block_parity(got, ref, what=f"{name}/{variant}")
 
 
-def test_ernie_as_drawn_block_full_size_sampled_rows():
+def test_ernie_as_drawn_block_full_size():
     """The ERNIE-shaped block as the page draws it, at full size, 74 valid text
     tokens (4096 + 74 = 4170 rows: ragged GEMM and attention tails) as when the
-    text is truncated to its valid length ([ERNIE] section VII, Decision 2)."""
+    text is truncated to its valid length ([ERNIE] section VII, Decision 2);
+    every row against the oracle's block (assert_full_size_parity)."""
     wl = with_variant(synth.WORKLOADS["ernie_block"], n_txt=74, **VARIANTS["ernie_as_drawn"])
     w = synth.block_weights(wl, 0, seed=0)
     x = synth.residual_input(wl, seed=1)
     mod_g, mod_o = conditioning_pair(wl, wl.t_block)
     got = run_block_gpu(wl, w, x, mod_g)
-    rows = sample_rows(wl.n_tokens)
-    ref = O.block_forward_rows(oracle_block_config(wl), oracle_weights(w), npf(x), mod_o,
-                               oracle_angles(wl), rows)
-    assert_block_parity(got[rows], ref, what="ernie_as_drawn 4170")
+    assert_full_size_parity(wl, w, x, got, mod_o, "ernie_as_drawn 4170")
 
 
 def test_block_truncated_text_4170_rows():
-    """The workload's block with the text truncated to 74 tokens: 4170 rows."""
+    """The workload's block with the text truncated to 74 tokens: 4170 rows,
+    every row against the oracle's block (assert_full_size_parity)."""
     wl = with_variant(synth.WORKLOADS["ernie_block"], n_txt=74)
     w = synth.block_weights(wl, 0, seed=0)
     x = synth.residual_input(wl, seed=1)
     mod_g, mod_o = conditioning_pair(wl, wl.t_block)
     got = run_block_gpu(wl, w, x, mod_g)
-    rows = sample_rows(wl.n_tokens)
-    ref = O.block_forward_rows(oracle_block_config(wl), oracle_weights(w), npf(x), mod_o,
-                               oracle_angles(wl), rows)
-    assert_block_parity(got[rows], ref, what="4170 rows")
+    assert_full_size_parity(wl, w, x, got, mod_o, "4170 rows")
 
 
 def test_block_zero_gates_pass_through_exactly():
@@ -271,6 +267,22 @@ def test_block_equals_its_stages():
     np.testing.assert_array_equal(npf(xs), npf(xb))
 
 
+def assert_full_size_parity(wl, w, x, got, mod_o, what):
+    """Every row of a full-size block against the oracle: max|err| within the
+    stated per-block bound, 2e-2 x RMS, or, where bf16 storage of the GEMM
+    inputs alone moves the worst element further than that, within 1.25 x
+    the error of an fp32 evaluation that rounds the same intermediates to
+    bf16 (built from oracle functions only)."""
+    cfg, ow, ang = oracle_block_config(wl), oracle_weights(w), oracle_angles(wl)
+    ref = O.block_forward(cfg, ow, npf(x), mod_o, ang, wl.n_seqs)
+    sim = bf16_storage_rows(cfg, ow, npf(x), mod_o, ang, np.arange(wl.n_tokens))
+    e_gpu, rms = max_err_vs_rms(got, ref)
+    e_sim, _ = max_err_vs_rms(sim, ref)
+    print(f"{what}: every row, max|err| {e_gpu / rms:.4f} x RMS, bf16 storage alone "
+          f"{e_sim / rms:.4f} x RMS")
+    assert e_gpu <= max(2e-2 * rms, 1.25 * e_sim + 1e-3 * rms), (e_gpu / rms, e_sim / rms)
+
+
 def sample_rows(n):
     rng = np.random.default_rng(11)
     return np.unique(np.concatenate([[0, 127, 128, n - 257, n - 256, n - 1],
@@ -278,20 +290,17 @@ def sample_rows(n):
 
 
 @pytest.mark.parametrize("name", ["ernie_block", "krea_gqa"])
-def test_block_forward_full_size_sampled_rows(name):
+def test_block_forward_full_size(name):
     """The 4352-token ERNIE-shaped block and the 1280-token Krea-shaped GQA
     block at full size, in the launch configuration the bench uses, with the
-    modulation of the timestep MLP at t = 0.5; the oracle computes 48 sampled
-    rows (image, text and tile-edge rows)."""
+    modulation of the timestep MLP at t = 0.5; every row against the oracle's
+    block (assert_full_size_parity)."""
     wl = synth.WORKLOADS[name]
     w = synth.block_weights(wl, 0, seed=0)
     x = synth.residual_input(wl, seed=1)
     mod_g, mod_o = conditioning_pair(wl, wl.t_block)
     got = run_block_gpu(wl, w, x, mod_g)
-    rows = sample_rows(wl.n_tokens)
-    ref = O.block_forward_rows(oracle_block_config(wl), oracle_weights(w), npf(x), mod_o,
-                               oracle_angles(wl), rows)
-    assert_block_parity(got[rows], ref, what=name)
+    assert_full_size_parity(wl, w, x, got, mod_o, name)
 
 
 @pytest.mark.parametrize("name", ["ernie_block", "krea_gqa"])
