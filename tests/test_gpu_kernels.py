@@ -12,11 +12,15 @@ pytestmark = pytest.mark.gpu
 
 dit = pytest.importorskip("diffusion_transformer_image_gb300.dit")
 
-BF16_REL = 2.0 ** -8   # one bf16 rounding of the output, with margin
+BF16_REL = 2.0 ** -8   # one bf16 rounding of the output: the unit roundoff of 8 significant bits
 
 
 def _rms(a):
     return float(np.sqrt(np.mean(np.asarray(a, np.float64) ** 2)))
+
+
+def _bf16(a):
+    return torch.from_numpy(np.ascontiguousarray(a, np.float32)).to(torch.bfloat16).float().numpy()
 
 
 # ------------------------------------------------------------------ GEMM
@@ -217,10 +221,23 @@ def test_attention(case):
     ref = O.attention(npf(q), npf(k), npf(v), nh, nkv, ns)
     got = npf(o)
     assert np.isfinite(got).all()
-    # The output is stored in bf16: rounding it alone moves an element by up
-    # to 2^-9 |o|, which for these heavy-tailed outputs is ~2 % of RMS(o) at
-    # the largest elements; P in bf16 adds an absolute term well below 1 %.
-    np.testing.assert_allclose(got, ref, rtol=BF16_REL, atol=1e-2 * _rms(ref))
+    rms = _rms(ref)
+    err = np.abs(got - ref)
+    rnd = np.abs(_bf16(ref) - ref)     # storing the exact output in bf16 alone
+    print(f"attention {case}: max|err| {err.max() / rms:.4f} x RMS, bf16 output rounding "
+          f"alone {rnd.max() / rms:.4f} x RMS, max|err| - rounding {(err - rnd).max() / rms:.4f} x RMS")
+    # Element by element, the rounding the kernel does: one bf16 rounding of
+    # the output (at most 2^-8 |o|, the unit roundoff of 8 significant bits)
+    # and P rounded to bf16 before the PV product.  A relative error of at
+    # most 2^-8 in every weight p_j moves o = sum p_j v_j / sum p_j by at most
+    # 2 * 2^-8 * sum p_j |v_j| / sum p_j, i.e. 2^-7 times attention over |v|.
+    p_bound = 2.0 ** -7 * O.attention(npf(q), npf(k), np.abs(npf(v)), nh, nkv, ns)
+    bound = BF16_REL * np.abs(ref) + p_bound
+    print(f"attention {case}: largest |err| / element bound {(err / bound).max():.3f}")
+    assert np.all(err <= bound + 1e-3 * rms), (err - bound).max() / rms
+    # The block bound, max|err| <= 2e-2 RMS(o), unless the bf16 rounding of
+    # the exact output alone already exceeds it (heavy-tailed rows).
+    assert err.max() <= max(2e-2 * rms, 1.25 * rnd.max() + 1e-3 * rms), (err.max() / rms, rnd.max() / rms)
 
 
 def test_bounded_wait_reports_timeout_and_context_survives():
