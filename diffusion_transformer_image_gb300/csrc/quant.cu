@@ -19,9 +19,15 @@
 //                       projections written once, in 8 bits
 // Both are persistent: a ring of whole rows in shared memory filled by one
 // TMA copy per row (128-byte swizzle, so that the reads below are free of
-// bank conflicts), one row per pass of the CTA, K / 32 threads, each owning
-// 32 consecutive values: spans 1..16 inside the thread (packed fp32 pairs
-// from span 2), spans 32, 64, 128 between the 8 threads of a 256-block.
+// bank conflicts), one row per pass of the CTA.  The normed rows take H / 32
+// threads, each owning 32 consecutive values: spans 1..16 inside the thread
+// (packed fp32 pairs from span 2), spans 32, 64, 128 between the 8 threads
+// of a 256-block.  The bf16 rows take K / 64 threads of 64 values (spans
+// 1..32 inside, 64 and 128 between 4 threads) when K is a multiple of 2048,
+// else K / 32 of 32: these kernels are bound by their instruction count and
+// per-row latency rather than by HBM, and an exchange span costs three
+// times an in-thread one per value.  The rotation's 1/16 is applied to the
+// scale instead of to every value (exactly equivalent, see fwht256_seg32).
 // One barrier per row for the bf16 rows (three for the normed rows: mean,
 // variance, maximum).  Rows whose K is not a multiple of 1024 (or too long)
 // take the warp-per-block kernels rotq_kernel / ln_rotq_kernel instead.
@@ -219,8 +225,13 @@ __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
                                     ~static_cast<uintptr_t>(1023));
 }
 
-// x H over this thread's 32 values (elements 32 j + e of a 256-block, j =
-// lane % 8), spans 1, 2, ..., 128 in order; then the exact scaling by 1/16.
+// 16 x H over this thread's 32 values (elements 32 j + e of a 256-block,
+// j = lane % 8), spans 1, 2, ..., 128 in order.  The 1/16 of H is left to
+// the coding step (code_seg32 / code_seg64): scaling every value of a row by
+// 2^4 scales its maximum, 448 / max and max / 448 by exact powers of two, so
+// the fp32 products value * (448 / max), hence the codes, and the scale
+// (multiplied by 1/16 at the end) are the same bits as with the scaling
+// done here, for every row whose values are normal floats.
 __device__ __forceinline__ void fwht256_seg32(float (&v)[32], int lane) {
 #pragma unroll
   for (int i = 0; i < 32; i += 2) {  // span 1
@@ -258,13 +269,58 @@ __device__ __forceinline__ void fwht256_seg32(float (&v)[32], int lane) {
       v[i + 1] = r.y;
     }
   }
-  const float2 sixteenth = make_float2(0.0625f, 0.0625f);
+}
+
+// The same for 64 values per thread (elements 64 j + e, j = lane % 4):
+// spans 1..32 inside the thread, 64 and 128 between the 4 lanes of a block.
+// Fewer instructions per element than 32 values per thread (one exchange
+// span less), which is what bounds these kernels.
+__device__ __forceinline__ void fwht256_seg64(float (&v)[64], int lane) {
 #pragma unroll
-  for (int i = 0; i < 32; i += 2) {
-    const float2 r = __fmul2_rn(make_float2(v[i], v[i + 1]), sixteenth);
-    v[i] = r.x;
-    v[i + 1] = r.y;
+  for (int i = 0; i < 64; i += 2) {  // span 1
+    const float a = v[i], b = v[i + 1];
+    v[i] = a + b;
+    v[i + 1] = a - b;
   }
+  const float2 neg1 = make_float2(-1.0f, -1.0f);
+#pragma unroll
+  for (int h = 1; h < 32; h <<= 1) {  // spans 2, 4, 8, 16, 32 on pairs (2j, 2j+1)
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      if (!(j & h)) {
+        const float2 a = make_float2(v[2 * j], v[2 * j + 1]);
+        const float2 b = make_float2(v[2 * (j + h)], v[2 * (j + h) + 1]);
+        const float2 s = __fadd2_rn(a, b);
+        const float2 d = __ffma2_rn(b, neg1, a);
+        v[2 * j] = s.x;
+        v[2 * j + 1] = s.y;
+        v[2 * (j + h)] = d.x;
+        v[2 * (j + h) + 1] = d.y;
+      }
+    }
+  }
+#pragma unroll
+  for (int m = 1; m < 4; m <<= 1) {  // spans 64, 128 between lanes
+    const float sg = (lane & m) ? -1.0f : 1.0f;
+    const float2 sg2 = make_float2(sg, sg);
+#pragma unroll
+    for (int i = 0; i < 64; i += 2) {
+      const float2 o = make_float2(__shfl_xor_sync(0xffffffffu, v[i], m),
+                                   __shfl_xor_sync(0xffffffffu, v[i + 1], m));
+      const float2 r = __ffma2_rn(sg2, make_float2(v[i], v[i + 1]), o);
+      v[i] = r.x;
+      v[i + 1] = r.y;
+    }
+  }
+}
+
+// max |v[i]| over an array, two values per three-input maximum
+template <int N>
+__device__ __forceinline__ float abs_max(const float (&v)[N]) {
+  float m = 0.0f;
+#pragma unroll
+  for (int i = 0; i < N; i += 2) m = fmax3(m, fabsf(v[i]), fabsf(v[i + 1]));
+  return m;
 }
 
 __device__ __forceinline__ float warp_max(float v) {
@@ -279,23 +335,28 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
-// Codes this thread's 32 rotated values with the row's maximum and stores
-// them (32 bytes) at dst; thread 0 stores the scale.
-__device__ __forceinline__ void code_seg32(const float (&v)[32], float amax, uint8_t* dst,
-                                           float* scale_out) {
-  const float inv = amax > 0.0f ? __fdiv_rn(448.0f, amax) : 0.0f;
-  if (threadIdx.x == 0) *scale_out = amax > 0.0f ? __fdiv_rn(amax, 448.0f) : 0.0f;
+// Codes this thread's N values of 16 x (x H) with the row's maximum amax16
+// of them and stores the N bytes at dst; thread 0 stores the scale
+// amax16 / 448 / 16 (see fwht256_seg32 for why the codes are those of x H).
+template <int N>
+__device__ __forceinline__ void code_seg(const float (&v)[N], float amax16, uint8_t* dst,
+                                         float* scale_out) {
+  const float inv = amax16 > 0.0f ? __fdiv_rn(448.0f, amax16) : 0.0f;
+  if (threadIdx.x == 0) *scale_out = amax16 > 0.0f ? __fdiv_rn(amax16, 448.0f) * 0.0625f : 0.0f;
   const float2 inv2 = make_float2(inv, inv);
-  uint32_t w[8];
-#pragma unroll
-  for (int q = 0; q < 8; ++q) {
-    const float2 a = __fmul2_rn(make_float2(v[4 * q], v[4 * q + 1]), inv2);
-    const float2 b = __fmul2_rn(make_float2(v[4 * q + 2], v[4 * q + 3]), inv2);
-    w[q] = pack_e4m3x4(a.x, a.y, b.x, b.y);
-  }
   uint4* d = reinterpret_cast<uint4*>(dst);
-  d[0] = make_uint4(w[0], w[1], w[2], w[3]);
-  d[1] = make_uint4(w[4], w[5], w[6], w[7]);
+#pragma unroll
+  for (int c = 0; c < N / 16; ++c) {
+    uint32_t w[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int i = 16 * c + 4 * q;
+      const float2 a = __fmul2_rn(make_float2(v[i], v[i + 1]), inv2);
+      const float2 b = __fmul2_rn(make_float2(v[i + 2], v[i + 3]), inv2);
+      w[q] = pack_e4m3x4(a.x, a.y, b.x, b.y);
+    }
+    d[c] = make_uint4(w[0], w[1], w[2], w[3]);
+  }
 }
 
 // Issues the TMA copy of row `row` into ring stage `s` (one elected thread).
@@ -312,10 +373,14 @@ __device__ __forceinline__ void rqt_drain(uint64_t* full, int first, int issued,
     mbar_wait(&full[n % RQT_STAGES], (uint32_t)((n / RQT_STAGES) & 1), e);
 }
 
-// bf16 rows [rows, K] (3-D map: 64 x K/64 x rows, box one row) -> codes.
-__global__ void __launch_bounds__(RQT_MAX_THREADS) rotq_tma_kernel(
+// bf16 rows [rows, K] (3-D map: 64 x K/64 x rows, box one row) -> codes,
+// K / VPT threads of VPT consecutive values each (VPT = 64 when K is a
+// multiple of 2048, else 32).
+template <int VPT>
+__global__ void __launch_bounds__(16384 / VPT) rotq_tma_kernel(
     const __grid_constant__ CUtensorMap tm, int rows, int K, uint8_t* __restrict__ q,
     long long ldq, float* __restrict__ scale, DevErr err) {
+  static_assert(VPT == 32 || VPT == 64, "32 or 64 values per thread");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   const int row_bytes = K * 2;
@@ -332,17 +397,19 @@ __global__ void __launch_bounds__(RQT_MAX_THREADS) rotq_tma_kernel(
       rqt_issue(smem, row_bytes, full, s, &tm, blockIdx.x + s * G);
   }
   __syncthreads();
-  // this thread's 64 bytes: half (t & 1) of 128-byte line t >> 1
-  const int L = t >> 1, half = t & 1;
+  // this thread's 2 VPT bytes: 16-byte chunks c0 .. c0 + VPT / 8 - 1 of the
+  // 128-byte line L (chunk c of line L sits at c ^ (L % 8): 128-byte swizzle)
+  constexpr int TPL = 64 / VPT;  // threads per line
+  const int L = t / TPL, c0 = (t % TPL) * (VPT / 8);
   int it = 0;
   for (int row = blockIdx.x; row < rows; row += G, ++it) {
     const int s = it % RQT_STAGES;
     const bool ok = mbar_wait(&full[s], (uint32_t)((it / RQT_STAGES) & 1), err);
-    float v[32];
+    float v[VPT];
     const uint8_t* line = smem + (size_t)s * row_bytes + (size_t)L * 128;
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const uint4 u = *reinterpret_cast<const uint4*>(line + (((half * 4 + k) ^ (L & 7)) << 4));
+    for (int k = 0; k < VPT / 8; ++k) {
+      const uint4 u = *reinterpret_cast<const uint4*>(line + (((c0 + k) ^ (L & 7)) << 4));
       const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
@@ -350,11 +417,11 @@ __global__ void __launch_bounds__(RQT_MAX_THREADS) rotq_tma_kernel(
         v[8 * k + 2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
       }
     }
-    fwht256_seg32(v, lane);
-    float m = 0.0f;
-#pragma unroll
-    for (int i = 0; i < 32; ++i) m = fmaxf(m, fabsf(v[i]));
-    m = warp_max(m);
+    if constexpr (VPT == 64)
+      fwht256_seg64(v, lane);
+    else
+      fwht256_seg32(v, lane);
+    float m = warp_max(abs_max(v));
     if (lane == 0) red[it & 1][warp] = m;
     // every thread has read stage s and published its maximum
     if (!__syncthreads_and(ok)) {
@@ -367,7 +434,7 @@ __global__ void __launch_bounds__(RQT_MAX_THREADS) rotq_tma_kernel(
     }
     float amax = red[it & 1][0];
     for (int w2 = 1; w2 < nwarps; ++w2) amax = fmaxf(amax, red[it & 1][w2]);
-    code_seg32(v, amax, q + (size_t)row * ldq + (size_t)t * 32, scale + row);
+    code_seg<VPT>(v, amax, q + (size_t)row * ldq + (size_t)t * VPT, scale + row);
   }
 }
 
@@ -458,15 +525,12 @@ __global__ void __launch_bounds__(RQT_LN_MAX_THREADS) ln_rotq_tma_kernel(
       v[i] = (MODE & 1) ? fmaf(n, pa[i], pb[i]) : fmaf(n, 1.0f + pb[i], pa[i]);
     }
     fwht256_seg32(v, lane);
-    float m = 0.0f;
-#pragma unroll
-    for (int i = 0; i < 32; ++i) m = fmaxf(m, fabsf(v[i]));
-    m = warp_max(m);
+    float m = warp_max(abs_max(v));
     if (lane == 0) red_m[warp] = m;
     __syncthreads();
     float amax = red_m[0];
     for (int w2 = 1; w2 < nwarps; ++w2) amax = fmaxf(amax, red_m[w2]);
-    code_seg32(v, amax, q + (size_t)row * ldq + (size_t)t * 32, scale + row);
+    code_seg<32>(v, amax, q + (size_t)row * ldq + (size_t)t * 32, scale + row);
   }
 }
 
@@ -478,7 +542,7 @@ size_t rqt_smem_bytes(int row_bytes) {
 // kernel variant and row length), times the SMs, at most one per row.
 template <typename Kern>
 cudaError_t rqt_grid(Kern kern, int variant, int threads, int row_bytes, int rows, int* grid) {
-  constexpr int MAXDEV = 64, VARIANTS = 5, LENGTHS = 33;
+  constexpr int MAXDEV = 64, VARIANTS = 6, LENGTHS = 33;
   static int occ[MAXDEV][VARIANTS][LENGTHS];
   static bool attr[MAXDEV][VARIANTS];
   const DeviceState* ds = device_state();
@@ -558,17 +622,23 @@ cudaError_t launch_rotate_quant(const __nv_bfloat16* x, long long ldx, int rows,
   if (rows < 0 || K <= 0 || K % 256 != 0 || K > ROTQ_MAX_K || ldx < K || ldq < K ||
       ldx % 8 != 0 || ldq % 16 != 0 || !aligned(x, 16) || !aligned(q, 16) || !aligned(scale, 4))
     return cudaErrorInvalidValue;
-  if (K % 1024 == 0) {  // the TMA-ring kernel: K / 32 threads, one 3-D copy per row
+  if (K % 1024 == 0) {  // the TMA-ring kernel: K / 64 or K / 32 threads, one 3-D copy per row
     CUtensorMap tm;
     const uint64_t dims[3] = {64, (uint64_t)K / 64, (uint64_t)rows};
     const uint64_t strides[2] = {128, (uint64_t)ldx * 2};
     const uint32_t box[3] = {64, (uint32_t)K / 64, 1};
     if (!make_tmap(&tm, 2, x, 3, dims, strides, box)) return cudaErrorInvalidValue;
     int grid = 0;
-    cudaError_t e = rqt_grid(rotq_tma_kernel, 0, K / 32, K * 2, rows, &grid);
-    if (e != cudaSuccess) return e;
-    rotq_tma_kernel<<<grid, K / 32, rqt_smem_bytes(K * 2), st>>>(tm, rows, K, q, ldq, scale,
-                                                                 dev_err(device_state()));
+    const DevErr err = dev_err(device_state());
+    if (K % 2048 == 0) {
+      cudaError_t e = rqt_grid(rotq_tma_kernel<64>, 5, K / 64, K * 2, rows, &grid);
+      if (e != cudaSuccess) return e;
+      rotq_tma_kernel<64><<<grid, K / 64, rqt_smem_bytes(K * 2), st>>>(tm, rows, K, q, ldq, scale, err);
+    } else {
+      cudaError_t e = rqt_grid(rotq_tma_kernel<32>, 0, K / 32, K * 2, rows, &grid);
+      if (e != cudaSuccess) return e;
+      rotq_tma_kernel<32><<<grid, K / 32, rqt_smem_bytes(K * 2), st>>>(tm, rows, K, q, ldq, scale, err);
+    }
     count_launch();
     return cudaGetLastError();
   }

@@ -51,7 +51,10 @@ def rows_input(rows, K, seed):
 
 
 # ------------------------------------------------------------- coding kernels
-@pytest.mark.parametrize("rows,K", [(1, 256), (37, 768), (130, 4096), (9, 12288), (3, 16384)])
+# K = 1024 and 3072 take 32 values per thread of the TMA-ring kernel, 2048
+# and up in steps of 2048 take 64, the rest the warp-per-block kernel.
+@pytest.mark.parametrize("rows,K", [(1, 256), (37, 768), (50, 3072), (130, 4096), (70, 6144),
+                                    (9, 12288), (3, 16384)])
 def test_rotate_quantize_bit_exact(rows, K):
     x = rows_input(rows, K, seed=rows + K)
     codes, scales = dit.dit_rotate_quantize(x.to(dev()))
