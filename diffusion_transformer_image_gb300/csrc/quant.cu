@@ -26,8 +26,7 @@
 // 1..32 inside, 64 and 128 between 4 threads) when K is a multiple of 2048,
 // else K / 32 of 32: these kernels are bound by their instruction count and
 // per-row latency rather than by HBM, and an exchange span costs three
-// times an in-thread one per value.  The rotation's 1/16 is applied to the
-// scale instead of to every value (exactly equivalent, see fwht256_seg32).
+// times an in-thread one per value.
 // One barrier per row for the bf16 rows (three for the normed rows: mean,
 // variance, maximum).  Rows whose K is not a multiple of 1024 (or too long)
 // take the warp-per-block kernels rotq_kernel / ln_rotq_kernel instead.
@@ -225,13 +224,22 @@ __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
                                     ~static_cast<uintptr_t>(1023));
 }
 
-// 16 x H over this thread's 32 values (elements 32 j + e of a 256-block,
-// j = lane % 8), spans 1, 2, ..., 128 in order.  The 1/16 of H is left to
-// the coding step (code_seg32 / code_seg64): scaling every value of a row by
-// 2^4 scales its maximum, 448 / max and max / 448 by exact powers of two, so
-// the fp32 products value * (448 / max), hence the codes, and the scale
-// (multiplied by 1/16 at the end) are the same bits as with the scaling
-// done here, for every row whose values are normal floats.
+// The exact scaling by 1/16 that ends the rotation, on packed pairs.  (It
+// stays a multiplication of every value: moving it to the row scale gives
+// the same bits only while the rotated values are normal floats.)
+template <int N>
+__device__ __forceinline__ void scale_sixteenth(float (&v)[N]) {
+  const float2 sixteenth = make_float2(0.0625f, 0.0625f);
+#pragma unroll
+  for (int i = 0; i < N; i += 2) {
+    const float2 r = __fmul2_rn(make_float2(v[i], v[i + 1]), sixteenth);
+    v[i] = r.x;
+    v[i + 1] = r.y;
+  }
+}
+
+// x H over this thread's 32 values (elements 32 j + e of a 256-block, j =
+// lane % 8), spans 1, 2, ..., 128 in order; then the exact scaling by 1/16.
 __device__ __forceinline__ void fwht256_seg32(float (&v)[32], int lane) {
 #pragma unroll
   for (int i = 0; i < 32; i += 2) {  // span 1
@@ -269,6 +277,7 @@ __device__ __forceinline__ void fwht256_seg32(float (&v)[32], int lane) {
       v[i + 1] = r.y;
     }
   }
+  scale_sixteenth(v);
 }
 
 // The same for 64 values per thread (elements 64 j + e, j = lane % 4):
@@ -312,6 +321,7 @@ __device__ __forceinline__ void fwht256_seg64(float (&v)[64], int lane) {
       v[i + 1] = r.y;
     }
   }
+  scale_sixteenth(v);
 }
 
 // max |v[i]| over an array, two values per three-input maximum
@@ -335,14 +345,13 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
-// Codes this thread's N values of 16 x (x H) with the row's maximum amax16
-// of them and stores the N bytes at dst; thread 0 stores the scale
-// amax16 / 448 / 16 (see fwht256_seg32 for why the codes are those of x H).
+// Codes this thread's N rotated values with the row's maximum and stores
+// the N bytes at dst; thread 0 stores the scale.
 template <int N>
-__device__ __forceinline__ void code_seg(const float (&v)[N], float amax16, uint8_t* dst,
+__device__ __forceinline__ void code_seg(const float (&v)[N], float amax, uint8_t* dst,
                                          float* scale_out) {
-  const float inv = amax16 > 0.0f ? __fdiv_rn(448.0f, amax16) : 0.0f;
-  if (threadIdx.x == 0) *scale_out = amax16 > 0.0f ? __fdiv_rn(amax16, 448.0f) * 0.0625f : 0.0f;
+  const float inv = amax > 0.0f ? __fdiv_rn(448.0f, amax) : 0.0f;
+  if (threadIdx.x == 0) *scale_out = amax > 0.0f ? __fdiv_rn(amax, 448.0f) : 0.0f;
   const float2 inv2 = make_float2(inv, inv);
   uint4* d = reinterpret_cast<uint4*>(dst);
 #pragma unroll

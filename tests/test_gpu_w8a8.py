@@ -64,6 +64,24 @@ def test_rotate_quantize_bit_exact(rows, K):
     np.testing.assert_array_equal(decode(codes), ref_codes)
 
 
+def test_rotate_quantize_extreme_scales():
+    """Rows scaled from 2^-120 to 2^100 on top of their own scales: codes and
+    scales bit-identical to the oracle's from tiny to huge rows, including a
+    row whose rotated values reach the subnormal range (the rotation's 1/16
+    is one exact multiplication of every value, as in the oracle; moving it
+    to the row scale would change such rows)."""
+    base = rows_input(8, 4096, seed=11).float()
+    f = torch.tensor([2.0 ** -100, 2.0 ** 100, 1.0, 2.0 ** -60, 2.0 ** 60, 2.0 ** -120, 3.0, 2.0 ** 90])
+    x = (base * f[:, None]).to(torch.bfloat16)
+    for K in (4096, 3072):   # 64 and 32 values per thread
+        xs = x[:, :K].contiguous()
+        codes, scales = dit.dit_rotate_quantize(xs.to(dev()))
+        torch.cuda.synchronize()
+        ref_codes, ref_scales = O.rotate_quantize(xs.float().numpy())
+        np.testing.assert_array_equal(npf(scales), ref_scales)
+        np.testing.assert_array_equal(decode(codes), ref_codes)
+
+
 def test_rotate_quantize_strided_rows():
     x = rows_input(20, 1024, seed=5)
     big = torch.zeros(20, 1024 + 64, dtype=torch.bfloat16)
