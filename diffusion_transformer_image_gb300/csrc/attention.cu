@@ -172,6 +172,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = bars->tmem_slot;
+  grid_dep_wait();  // q, k and v of the projection before are complete
+  grid_dep_launch();
 
   if (warp == 0) {
     if (lane == 0) {
@@ -422,9 +424,7 @@ cudaError_t launch_hd(const CUtensorMap& tq, const CUtensorMap& tv, const AttnPa
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
-  attn_kernel<HD><<<grid, NUM_THREADS, attn_smem_bytes<HD>(), st>>>(tq, tv, p);
-  count_launch();
-  return cudaGetLastError();
+  return launch_k(attn_kernel<HD>, grid, dim3(NUM_THREADS), attn_smem_bytes<HD>(), st, 1, tq, tv, p);
 }
 
 }  // namespace

@@ -40,6 +40,22 @@ __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
                : "memory");
 }
 
+// Programmatic dependent launch.  Every kernel of the library is launched
+// with programmatic stream serialization, so its CTAs may be scheduled while
+// the kernel before it in the stream is still finishing.  grid_dep_wait()
+// returns once that kernel has completed and its memory operations are
+// visible; each kernel calls it in every CTA before it reads or writes any
+// global memory (shared memory, barriers and tensor memory may be set up
+// before), so the stream order of all global accesses is unchanged, and
+// because every CTA waits, a kernel completes only after its predecessor
+// has.  grid_dep_launch() then allows the next kernel's CTAs to be
+// scheduled; a kernel allocates its tensor memory before it, so a CTA that
+// is scheduled early can never hold columns a running CTA still needs.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ void fence_barrier_init() {
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }

@@ -689,6 +689,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   cluster_sync();  // both CTAs' barriers exist before either signals the other
   tc_fence_after();
   const uint32_t tmem_base = bars->tmem_slot;
+  grid_dep_wait();  // the previous kernel's outputs (A, the residual x) are complete
+  grid_dep_launch();
 
   if (warp == 0) {
     if (lane == 0) {
@@ -846,10 +848,8 @@ cudaError_t launch_impl(const CUtensorMap& ta, const CUtensorMap& tb, const CUte
     max_pairs[dev] = n < 1 ? 1 : n;
   }
   const int pairs = tiles < max_pairs[dev] ? tiles : max_pairs[dev];
-  cfg.gridDim = dim3(2 * pairs, 1, 1);
-  cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_kernel<EPI, HD, F8>, ta, tb, to, tv, p);
-  count_launch();
-  return e != cudaSuccess ? e : cudaGetLastError();
+  return launch_k(gemm_kernel<EPI, HD, F8>, dim3(2 * pairs, 1, 1), dim3(NUM_THREADS, 1, 1),
+                  smem_bytes<EPI>(), st, 2, ta, tb, to, tv, p);
 }
 
 // Encodes the two operand maps (boxes of 128 bytes of K by 128 rows), counts

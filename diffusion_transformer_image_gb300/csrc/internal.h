@@ -21,6 +21,36 @@ const DeviceState* device_state();  // nullptr if CUDA is unusable
 inline DevErr dev_err(const DeviceState* ds) { return DevErr{ds->err, ds->timeout_ns}; }
 void count_launch(int n = 1);
 
+// Launches a kernel with programmatic stream serialization (see
+// grid_dep_wait in common.cuh): the launch of the next kernel overlaps the
+// tail of the one before it.  cluster_x > 1 adds a cluster dimension.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_k(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                     int cluster_x, Args... args) {
+  cudaLaunchAttribute attr[2];
+  int n = 0;
+  attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[n].val.programmaticStreamSerializationAllowed = 1;
+  ++n;
+  if (cluster_x > 1) {
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = (unsigned)cluster_x;
+    attr[n].val.clusterDim.y = 1;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = (unsigned)n;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+  count_launch();
+  return e != cudaSuccess ? e : cudaGetLastError();
+}
+
 // Encodes a row-major tensor map with 128-byte swizzle (or none): bf16
 // elements (elem_bytes 2), fp32 (4) or bytes (1, the e4m3 codes).
 // dims[0] is the contiguous dimension; strides_bytes has rank-1 entries.

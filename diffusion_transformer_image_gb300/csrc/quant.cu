@@ -125,6 +125,8 @@ __global__ void __launch_bounds__(RQ_THREADS) rotq_kernel(const __nv_bfloat16* _
                                                           uint8_t* __restrict__ q, long long ldq,
                                                           float* __restrict__ scale) {
   __shared__ float red[RQ_WARPS];
+  grid_dep_wait();
+  grid_dep_launch();
   const int row = blockIdx.x;
   if (row >= rows) return;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -156,6 +158,8 @@ __global__ void __launch_bounds__(RQ_THREADS) ln_rotq_kernel(
     const float* __restrict__ p1, float eps, uint8_t* __restrict__ q, long long ldq,
     float* __restrict__ scale) {
   __shared__ float red[RQ_WARPS];
+  grid_dep_wait();
+  grid_dep_launch();
   const int row = blockIdx.x;
   if (row >= rows) return;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -398,6 +402,8 @@ __global__ void __launch_bounds__(16384 / VPT) rotq_tma_kernel(
   const int t = threadIdx.x, warp = t >> 5, lane = t & 31, nwarps = blockDim.x >> 5;
   const int G = gridDim.x;
   int issued = 0;  // rows of this CTA whose copy has been issued (thread 0)
+  grid_dep_wait();
+  grid_dep_launch();
   if (t == 0) {
     for (int s = 0; s < RQT_STAGES; ++s) mbar_init(&full[s], 1);
     fence_barrier_init();
@@ -464,6 +470,8 @@ __global__ void __launch_bounds__(RQT_LN_MAX_THREADS) ln_rotq_tma_kernel(
   const int t = threadIdx.x, warp = t >> 5, lane = t & 31, nwarps = blockDim.x >> 5;
   const int G = gridDim.x;
   int issued = 0;
+  grid_dep_wait();
+  grid_dep_launch();
   if (t == 0) {
     for (int s = 0; s < RQT_STAGES; ++s) mbar_init(&full[s], 1);
     fence_barrier_init();
@@ -587,10 +595,9 @@ cudaError_t ln_rotq_tma_launch(const CUtensorMap& tm, int rows, int H, const flo
   cudaError_t e = rqt_grid(ln_rotq_tma_kernel<MODE, RMS>, 1 + MODE + (RMS ? 2 : 0), threads,
                            row_bytes, rows, &grid);
   if (e != cudaSuccess) return e;
-  ln_rotq_tma_kernel<MODE, RMS><<<grid, threads, rqt_smem_bytes(row_bytes), st>>>(
-      tm, rows, H, p0, p1, eps, q, ldq, scale, dev_err(device_state()));
-  count_launch();
-  return cudaGetLastError();
+  return launch_k(ln_rotq_tma_kernel<MODE, RMS>, dim3(grid), dim3(threads),
+                  rqt_smem_bytes(row_bytes), st, 1, tm, rows, H, p0, p1, eps, q, ldq, scale,
+                  dev_err(device_state()));
 }
 
 bool aligned(const void* p, unsigned a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
@@ -598,19 +605,16 @@ bool aligned(const void* p, unsigned a) { return (reinterpret_cast<uintptr_t>(p)
 template <int MAXC>
 cudaError_t rotq_launch(const __nv_bfloat16* x, long long ldx, int rows, int K, uint8_t* q,
                         long long ldq, float* scale, cudaStream_t st) {
-  rotq_kernel<MAXC><<<rows, RQ_THREADS, 0, st>>>(x, ldx, rows, K, q, ldq, scale);
-  count_launch();
-  return cudaGetLastError();
+  return launch_k(rotq_kernel<MAXC>, dim3(rows), dim3(RQ_THREADS), 0, st, 1, x, ldx, rows, K, q,
+                  ldq, scale);
 }
 
 template <int MODE, bool RMS, int MAXC>
 cudaError_t ln_rotq_launch(const float* x, long long ldx, int rows, int H, const float* p0,
                            const float* p1, float eps, uint8_t* q, long long ldq, float* scale,
                            cudaStream_t st) {
-  ln_rotq_kernel<MODE, RMS, MAXC>
-      <<<rows, RQ_THREADS, 0, st>>>(x, ldx, rows, H, p0, p1, eps, q, ldq, scale);
-  count_launch();
-  return cudaGetLastError();
+  return launch_k(ln_rotq_kernel<MODE, RMS, MAXC>, dim3(rows), dim3(RQ_THREADS), 0, st, 1, x,
+                  ldx, rows, H, p0, p1, eps, q, ldq, scale);
 }
 
 template <int MODE, bool RMS>
@@ -642,14 +646,13 @@ cudaError_t launch_rotate_quant(const __nv_bfloat16* x, long long ldx, int rows,
     if (K % 2048 == 0) {
       cudaError_t e = rqt_grid(rotq_tma_kernel<64>, 5, K / 64, K * 2, rows, &grid);
       if (e != cudaSuccess) return e;
-      rotq_tma_kernel<64><<<grid, K / 64, rqt_smem_bytes(K * 2), st>>>(tm, rows, K, q, ldq, scale, err);
-    } else {
-      cudaError_t e = rqt_grid(rotq_tma_kernel<32>, 0, K / 32, K * 2, rows, &grid);
-      if (e != cudaSuccess) return e;
-      rotq_tma_kernel<32><<<grid, K / 32, rqt_smem_bytes(K * 2), st>>>(tm, rows, K, q, ldq, scale, err);
+      return launch_k(rotq_tma_kernel<64>, dim3(grid), dim3(K / 64), rqt_smem_bytes(K * 2), st, 1,
+                      tm, rows, K, q, ldq, scale, err);
     }
-    count_launch();
-    return cudaGetLastError();
+    cudaError_t e = rqt_grid(rotq_tma_kernel<32>, 0, K / 32, K * 2, rows, &grid);
+    if (e != cudaSuccess) return e;
+    return launch_k(rotq_tma_kernel<32>, dim3(grid), dim3(K / 32), rqt_smem_bytes(K * 2), st, 1,
+                    tm, rows, K, q, ldq, scale, err);
   }
   const int per_warp = (K / 256 + RQ_WARPS - 1) / RQ_WARPS;
   if (per_warp <= 1) return rotq_launch<1>(x, ldx, rows, K, q, ldq, scale, st);

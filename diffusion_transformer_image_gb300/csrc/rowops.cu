@@ -45,6 +45,8 @@ __global__ void __launch_bounds__(LN_THREADS) ln_modulate_kernel(
     const float* __restrict__ x, long long ldx, int rows, int H, const float* __restrict__ p0,
     const float* __restrict__ p1, float eps, __nv_bfloat16* __restrict__ out, long long ldo,
     __nv_bfloat16* __restrict__ out_lo) {
+  grid_dep_wait();
+  grid_dep_launch();
   __shared__ float red[LN_WARPS];
   const int row = blockIdx.x;
   if (row >= rows) return;
@@ -129,6 +131,8 @@ __global__ void __launch_bounds__(LNW_WARPS * 32) ln_modulate_warp_kernel(
     const float* __restrict__ x, long long ldx, int rows, const float* __restrict__ p0,
     const float* __restrict__ p1, float eps, __nv_bfloat16* __restrict__ out, long long ldo,
     __nv_bfloat16* __restrict__ out_lo) {
+  grid_dep_wait();
+  grid_dep_launch();
   constexpr int H = 128 * NV;
   const int row = blockIdx.x * LNW_WARPS + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
@@ -190,6 +194,8 @@ __global__ void __launch_bounds__(LNW_WARPS * 32) ln_modulate_warp_kernel(
 // ([ZFLOW] section IV, Euler sign +1).
 __global__ void euler_kernel(float* __restrict__ x, const float* __restrict__ v, long long n,
                              float dt) {
+  grid_dep_wait();
+  grid_dep_launch();
   const long long n4 = n >> 2;
   const long long stride = (long long)gridDim.x * blockDim.x;
   float4* x4 = reinterpret_cast<float4*>(x);
@@ -219,6 +225,8 @@ __global__ void __launch_bounds__(256) gemv_kernel(const __nv_bfloat16* __restri
                                                    const float* __restrict__ b,
                                                    float* __restrict__ y, int O, int K,
                                                    int silu_in) {
+  grid_dep_wait();
+  grid_dep_launch();
   extern __shared__ float xs[];
   for (int k = threadIdx.x; k < K; k += blockDim.x) {
     const float t = x[k];
@@ -254,6 +262,8 @@ __global__ void __launch_bounds__(256) gemv_kernel(const __nv_bfloat16* __restri
 // e = [cos(T w_j), sin(T w_j)], w_j = 10000^(-j / half), cosine half first
 // ([ZFLOW] section IV: flip_sin_to_cos).
 __global__ void sinusoid_kernel(float T, int dim, float* out) {
+  grid_dep_wait();
+  grid_dep_launch();
   const int half = dim / 2;
   for (int j = threadIdx.x; j < half; j += blockDim.x) {
     const float w = (float)exp(-log(10000.0) * (double)j / (double)half);
@@ -278,6 +288,8 @@ struct Axes3 {
 __global__ void rope_grid_kernel(int grid_h, int grid_w, int n_txt, const int* __restrict__ pos,
                                  int n, Axes3 axes, float theta, int half_d,
                                  float* __restrict__ cos_out, float* __restrict__ sin_out) {
+  grid_dep_wait();
+  grid_dep_launch();
   const long long total = (long long)n * half_d;
   const int n_img = grid_h * grid_w;
   for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total;
@@ -318,6 +330,8 @@ __global__ void rope_grid_kernel(int grid_h, int grid_w, int n_txt, const int* _
 // w_k = base^(-k / (d/4)).  Pair-major like the grid tables.
 __global__ void rope_vit_kernel(int grid_h, int grid_w, int n_prefix, int head_dim, float base,
                                 float* __restrict__ cos_out, float* __restrict__ sin_out) {
+  grid_dep_wait();
+  grid_dep_launch();
   const int half = head_dim / 2, q = head_dim / 4;
   const long long n = (long long)n_prefix + (long long)grid_h * grid_w;
   for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n * half;
@@ -340,6 +354,8 @@ __global__ void rope_vit_kernel(int grid_h, int grid_w, int n_prefix, int head_d
 // ------------------------------------------------------------------- casts
 __global__ void f32_to_bf16_kernel(const float* __restrict__ in, __nv_bfloat16* __restrict__ out,
                                    long long n) {
+  grid_dep_wait();
+  grid_dep_launch();
   const long long n4 = n >> 2;
   for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n4;
        i += (long long)gridDim.x * blockDim.x) {
@@ -357,6 +373,8 @@ __global__ void f32_to_bf16_kernel(const float* __restrict__ in, __nv_bfloat16* 
 // bf16 operands.
 __global__ void split_bf16_kernel(const float* __restrict__ in, __nv_bfloat16* __restrict__ hi,
                                   __nv_bfloat16* __restrict__ lo, long long n) {
+  grid_dep_wait();
+  grid_dep_launch();
   for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n;
        i += (long long)gridDim.x * blockDim.x) {
     const float x = in[i];
@@ -368,6 +386,8 @@ __global__ void split_bf16_kernel(const float* __restrict__ in, __nv_bfloat16* _
 
 __global__ void bf16_to_f32_kernel(const __nv_bfloat16* __restrict__ in, float* __restrict__ out,
                                    long long n) {
+  grid_dep_wait();
+  grid_dep_launch();
   for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n;
        i += (long long)gridDim.x * blockDim.x)
     out[i] = __bfloat162float(in[i]);
@@ -375,6 +395,8 @@ __global__ void bf16_to_f32_kernel(const __nv_bfloat16* __restrict__ in, float* 
 
 // A wait that nothing completes: exercises the bounded-wait failure path.
 __global__ void stuck_wait_kernel(DevErr e) {
+  grid_dep_wait();
+  grid_dep_launch();
   __shared__ uint64_t bar;
   if (threadIdx.x == 0) {
     mbar_init(&bar, 1);
@@ -404,48 +426,42 @@ cudaError_t launch_ln_modulate(int mode, const float* x, long long ldx, int rows
   // widths the warp-per-row kernel is built for
   if (H == 1024 || H == 256) {
     const int g = (rows + LNW_WARPS - 1) / LNW_WARPS;
-#define DIT_LNW(M, R, NV)                                                                \
-  ln_modulate_warp_kernel<M, R, NV><<<g, LNW_WARPS * 32, 0, st>>>(x, ldx, rows, p0, p1, eps, out, \
-                                                                  ldo, out_lo)
-#define DIT_LNW_H(M, R) (H == 1024 ? DIT_LNW(M, R, 8) : DIT_LNW(M, R, 2))
+#define DIT_LNW(M, R, NV)                                                                    \
+  launch_k(ln_modulate_warp_kernel<M, R, NV>, dim3(g), dim3(LNW_WARPS * 32), 0, st, 1, x, ldx, \
+           rows, p0, p1, eps, out, ldo, out_lo)
+#define DIT_LNW_H(M, R) return (H == 1024 ? DIT_LNW(M, R, 8) : DIT_LNW(M, R, 2))
     switch (mode) {
-      case 0: DIT_LNW_H(0, false); break;
-      case 1: DIT_LNW_H(1, false); break;
-      case 2: DIT_LNW_H(0, true); break;
-      case 3: DIT_LNW_H(1, true); break;
+      case 0: DIT_LNW_H(0, false);
+      case 1: DIT_LNW_H(1, false);
+      case 2: DIT_LNW_H(0, true);
+      case 3: DIT_LNW_H(1, true);
       default: return cudaErrorInvalidValue;
     }
 #undef DIT_LNW_H
 #undef DIT_LNW
-    count_launch();
-    return cudaGetLastError();
   }
   const bool small = H <= LN_THREADS * 4 * 4;
-#define DIT_LN_LAUNCH(M, R)                                                                     \
-  (small ? (ln_modulate_kernel<M, R, 4><<<grid, LN_THREADS, 0, st>>>(x, ldx, rows, H, p0, p1, eps, \
-                                                                     out, ldo, out_lo), 0)          \
-         : (ln_modulate_kernel<M, R, LN_MAXV><<<grid, LN_THREADS, 0, st>>>(x, ldx, rows, H, p0, p1, \
-                                                                           eps, out, ldo, out_lo), \
-            0))
+#define DIT_LN_LAUNCH(M, R)                                                                  \
+  return small ? launch_k(ln_modulate_kernel<M, R, 4>, dim3(grid), dim3(LN_THREADS), 0, st, 1, \
+                          x, ldx, rows, H, p0, p1, eps, out, ldo, out_lo)                   \
+               : launch_k(ln_modulate_kernel<M, R, LN_MAXV>, dim3(grid), dim3(LN_THREADS), 0,  \
+                          st, 1, x, ldx, rows, H, p0, p1, eps, out, ldo, out_lo)
   switch (mode) {
-    case 0: DIT_LN_LAUNCH(0, false); break;
-    case 1: DIT_LN_LAUNCH(1, false); break;
-    case 2: DIT_LN_LAUNCH(0, true); break;
-    case 3: DIT_LN_LAUNCH(1, true); break;
+    case 0: DIT_LN_LAUNCH(0, false);
+    case 1: DIT_LN_LAUNCH(1, false);
+    case 2: DIT_LN_LAUNCH(0, true);
+    case 3: DIT_LN_LAUNCH(1, true);
     default: return cudaErrorInvalidValue;
   }
 #undef DIT_LN_LAUNCH
-  count_launch();
-  return cudaGetLastError();
 }
 
 cudaError_t launch_euler(float* x, const float* v, long long n, float dt, cudaStream_t st) {
   const DeviceState* ds = device_state();
   if (!ds) return cudaErrorInitializationError;
   if (n == 0) return cudaSuccess;
-  euler_kernel<<<grid_for((n + 3) / 4, 256, ds->sm_count), 256, 0, st>>>(x, v, n, dt);
-  count_launch();
-  return cudaGetLastError();
+  return launch_k(euler_kernel, dim3(grid_for((n + 3) / 4, 256, ds->sm_count)), dim3(256), 0, st,
+                  1, x, v, n, dt);
 }
 
 cudaError_t launch_gemv(const __nv_bfloat16* W, const float* x, const float* b, float* y, int O,
@@ -465,15 +481,11 @@ cudaError_t launch_gemv(const __nv_bfloat16* W, const float* x, const float* b, 
       attr_set[dev] = true;
     }
   }
-  gemv_kernel<<<grid, 256, smem, st>>>(W, x, b, y, O, K, silu_in);
-  count_launch();
-  return cudaGetLastError();
+  return launch_k(gemv_kernel, dim3(grid), dim3(256), smem, st, 1, W, x, b, y, O, K, silu_in);
 }
 
 cudaError_t launch_sinusoid(float T, int dim, float* out, cudaStream_t st) {
-  sinusoid_kernel<<<1, 128, 0, st>>>(T, dim, out);
-  count_launch();
-  return cudaGetLastError();
+  return launch_k(sinusoid_kernel, dim3(1), dim3(128), 0, st, 1, T, dim, out);
 }
 
 cudaError_t launch_rope_grid(int grid_h, int grid_w, int n_txt, const int* pos, int n_pos,
@@ -484,11 +496,9 @@ cudaError_t launch_rope_grid(int grid_h, int grid_w, int n_txt, const int* pos, 
   const int n = pos ? n_pos : grid_h * grid_w + n_txt;
   const long long total = (long long)n * half_d;
   if (total == 0) return cudaSuccess;
-  rope_grid_kernel<<<grid_for(total, 256, ds->sm_count), 256, 0, st>>>(
-      grid_h, grid_w, n_txt, pos, n, Axes3{axes[0], axes[1], axes[2]}, theta, half_d, cos_out,
-      sin_out);
-  count_launch();
-  return cudaGetLastError();
+  return launch_k(rope_grid_kernel, dim3(grid_for(total, 256, ds->sm_count)), dim3(256), 0, st, 1,
+                  grid_h, grid_w, n_txt, pos, n, Axes3{axes[0], axes[1], axes[2]}, theta, half_d,
+                  cos_out, sin_out);
 }
 
 cudaError_t launch_rope_vit(int grid_h, int grid_w, int n_prefix, int head_dim, float base,
@@ -497,19 +507,16 @@ cudaError_t launch_rope_vit(int grid_h, int grid_w, int n_prefix, int head_dim, 
   if (!ds) return cudaErrorInitializationError;
   const long long total = ((long long)n_prefix + (long long)grid_h * grid_w) * (head_dim / 2);
   if (total == 0) return cudaSuccess;
-  rope_vit_kernel<<<grid_for(total, 256, ds->sm_count), 256, 0, st>>>(
-      grid_h, grid_w, n_prefix, head_dim, base, cos_out, sin_out);
-  count_launch();
-  return cudaGetLastError();
+  return launch_k(rope_vit_kernel, dim3(grid_for(total, 256, ds->sm_count)), dim3(256), 0, st, 1,
+                  grid_h, grid_w, n_prefix, head_dim, base, cos_out, sin_out);
 }
 
 cudaError_t launch_f32_to_bf16(const float* in, __nv_bfloat16* out, long long n, cudaStream_t st) {
   const DeviceState* ds = device_state();
   if (!ds) return cudaErrorInitializationError;
   if (n == 0) return cudaSuccess;
-  f32_to_bf16_kernel<<<grid_for((n + 3) / 4, 256, ds->sm_count), 256, 0, st>>>(in, out, n);
-  count_launch();
-  return cudaGetLastError();
+  return launch_k(f32_to_bf16_kernel, dim3(grid_for((n + 3) / 4, 256, ds->sm_count)), dim3(256),
+                  0, st, 1, in, out, n);
 }
 
 cudaError_t launch_split_bf16(const float* in, __nv_bfloat16* hi, __nv_bfloat16* lo, long long n,
@@ -517,24 +524,20 @@ cudaError_t launch_split_bf16(const float* in, __nv_bfloat16* hi, __nv_bfloat16*
   const DeviceState* ds = device_state();
   if (!ds) return cudaErrorInitializationError;
   if (n == 0) return cudaSuccess;
-  split_bf16_kernel<<<grid_for(n, 256, ds->sm_count), 256, 0, st>>>(in, hi, lo, n);
-  count_launch();
-  return cudaGetLastError();
+  return launch_k(split_bf16_kernel, dim3(grid_for(n, 256, ds->sm_count)), dim3(256), 0, st, 1,
+                  in, hi, lo, n);
 }
 
 cudaError_t launch_bf16_to_f32(const __nv_bfloat16* in, float* out, long long n, cudaStream_t st) {
   const DeviceState* ds = device_state();
   if (!ds) return cudaErrorInitializationError;
   if (n == 0) return cudaSuccess;
-  bf16_to_f32_kernel<<<grid_for(n, 256, ds->sm_count), 256, 0, st>>>(in, out, n);
-  count_launch();
-  return cudaGetLastError();
+  return launch_k(bf16_to_f32_kernel, dim3(grid_for(n, 256, ds->sm_count)), dim3(256), 0, st, 1,
+                  in, out, n);
 }
 
 cudaError_t launch_stuck_wait(DevErr e, cudaStream_t st) {
-  stuck_wait_kernel<<<1, 32, 0, st>>>(e);
-  count_launch();
-  return cudaGetLastError();
+  return launch_k(stuck_wait_kernel, dim3(1), dim3(32), 0, st, 1, e);
 }
 
 }  // namespace dit
