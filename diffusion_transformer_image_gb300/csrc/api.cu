@@ -219,11 +219,14 @@ BlockWs block_ws_layout(const dit_block_config* c, int n_tokens, int n_seqs, voi
 }
 
 // a: bf16 rows, or e4m3 codes with row scales a_scale (W8A8 format).
+// b_early: the GEMM follows another kernel of the same call (see GemmParams).
 dit_status run_qkv(const dit_block_config* c, const dit_block_weights* w, const void* a,
                    const float* a_scale, int n_tokens, int n_seqs, const float* rc,
-                   const float* rs, __nv_bfloat16* qk, __nv_bfloat16* vt, cudaStream_t st) {
+                   const float* rs, __nv_bfloat16* qk, __nv_bfloat16* vt, cudaStream_t st,
+                   bool b_early = false) {
   const int hd = c->head_dim;
   GemmParams p{};
+  p.b_early = b_early ? 1 : 0;
   p.M = n_tokens;
   p.N = (c->n_heads + 2 * c->n_kv_heads) * hd;
   p.K = c->hidden;
@@ -287,8 +290,11 @@ dit_status block_forward_impl(const dit_block_config* c, const dit_block_weights
   const void* a_op = q8 ? static_cast<const void*>(ws.a8) : ws.a;
   e = norm_rows(ada ? mod : w->ln1_g, ada ? mod + H : w->ln1_b);
   if (e != cudaSuccess) return DIT_ECUDA;
+  // The block's projections follow another kernel of this call, and only
+  // the caller writes the weights (before the call): their B tiles may be
+  // requested before the grid-dependency wait.
   dit_status s = run_qkv(c, w, a_op, q8 ? ws.sa : nullptr, n_tokens, n_seqs, rc, rs, ws.qk,
-                         ws.vt, st);
+                         ws.vt, st, true);
   if (s != DIT_OK) return s;
   e = launch_attention(hd, ws.qk, ws.vt, n_tokens, n_seqs, c->n_heads, c->n_kv_heads, ws.o, st);
   if (e != cudaSuccess) return DIT_ECUDA;
@@ -302,6 +308,7 @@ dit_status block_forward_impl(const dit_block_config* c, const dit_block_weights
     p.out = x;
     p.ldo = H;
     p.vec = ada ? mod + 2 * H : nullptr;
+    p.b_early = 1;
     e = project(residual_epi(ada ? c->gate_fn : 0), q8 ? (const void*)ws.o8 : ws.o,
                 q8 ? ws.so : nullptr, HQ, w->w_o, w->w_o_scale, HQ, p, st);
     if (e != cudaSuccess) return DIT_ECUDA;
@@ -315,6 +322,7 @@ dit_status block_forward_impl(const dit_block_config* c, const dit_block_weights
     p.K = H;
     p.out = ws.h;
     p.ldo = F;
+    p.b_early = 1;
     e = project(c->glu_act ? EPI_GEGLU : EPI_SWIGLU, a_op, q8 ? ws.sa : nullptr, H, w->w_gu,
                 w->w_gu_scale, H, p, st);
     if (e != cudaSuccess) return DIT_ECUDA;
@@ -329,6 +337,7 @@ dit_status block_forward_impl(const dit_block_config* c, const dit_block_weights
     p.out = x;
     p.ldo = H;
     p.vec = ada ? mod + 5 * H : nullptr;
+    p.b_early = 1;
     e = project(residual_epi(ada ? c->gate_fn : 0), q8 ? (const void*)ws.h8 : ws.h,
                 q8 ? ws.sh : nullptr, F, w->w_down, w->w_down_scale, F, p, st);
     if (e != cudaSuccess) return DIT_ECUDA;

@@ -689,6 +689,23 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   cluster_sync();  // both CTAs' barriers exist before either signals the other
   tc_fence_after();
   const uint32_t tmem_base = bars->tmem_slot;
+  // With p.b_early the producer requests the B tiles of its first tile's
+  // first stages (fresh stages: no empty wait) before the grid-dependency
+  // wait, so that they load while the kernel before this one finishes.
+  int b_pre = 0;
+  if (p.b_early && warp == 0 && lane == 0) {
+    int m_blk, n_blk;
+    tile_coords(p, pair, m_blk, n_blk);
+    const int b_row = (EPI == EPI_SWIGLU || EPI == EPI_GEGLU)
+                          ? (rank ? p.N : 0) + n_blk * BNH
+                          : n_blk * BN + (int)rank * BNH;
+    b_pre = k_blocks < STAGES ? k_blocks : STAGES;
+    for (int kb = 0; kb < b_pre; ++kb) {
+      if (rank == 0) mbar_arrive_expect_tx(&bars->full[kb], 2 * STAGE_BYTES);
+      tma_load_2d_pair(smem + (size_t)kb * STAGE_BYTES + A_BYTES, &tmB,
+                       mapa_shared(smem_u32(&bars->full[kb]), 0), kb * BK, b_row);
+    }
+  }
   grid_dep_wait();  // the previous kernel's outputs (A, the residual x) are complete
   grid_dep_launch();
 
@@ -707,20 +724,22 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                               ? (rank ? p.N : 0) + n_blk * BNH
                               : n_blk * BN + (int)rank * BNH;
         for (int kb = 0; kb < k_blocks; ++kb) {
-          if (!mbar_wait(&bars->empty[stage], phase ^ 1u, p.err)) {
+          // the first tile's first b_pre stages: B already requested
+          const bool pre = t == pair && kb < b_pre;
+          if (!pre && !mbar_wait(&bars->empty[stage], phase ^ 1u, p.err)) {
             ok = false;
             break;
           }
           uint8_t* sa = smem + (size_t)stage * STAGE_BYTES;
           uint8_t* sb = sa + A_BYTES;
           if (rank == 0) {
-            mbar_arrive_expect_tx(&bars->full[stage], 2 * STAGE_BYTES);
+            if (!pre) mbar_arrive_expect_tx(&bars->full[stage], 2 * STAGE_BYTES);
             filled |= 1u << stage;
             fill_parity = (fill_parity & ~(1u << stage)) | (phase << stage);
           }
           const uint32_t fb = mapa_shared(smem_u32(&bars->full[stage]), 0);
           tma_load_2d_pair(sa, &tmA, fb, kb * BK, a_row);
-          tma_load_2d_pair(sb, &tmB, fb, kb * BK, b_row);
+          if (!pre) tma_load_2d_pair(sb, &tmB, fb, kb * BK, b_row);
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;

@@ -101,6 +101,13 @@ struct GemmParams {
   QkvEpi qkv;
   DevErr err;
   int group_m;          // row blocks per raster group (tiles walk rows fastest inside one)
+  // B is not written by the kernel launched just before this one in the
+  // stream (the projections inside a block, whose weights only the caller
+  // writes, before the block's first kernel): the producer may request the
+  // first stages' B tiles before the grid-dependency wait.  Such a GEMM
+  // starts only once every CTA of the kernel before it has passed its own
+  // wait, i.e. once everything earlier has completed.
+  int b_early;
 };
 
 // D = A[M,K] B[rows,K]^T with the epilogue `epi`; hd selects the QKV head
